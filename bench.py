@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Benchmark of hc_mix_fused (hyper-connection mix statistics + Sinkhorn) at M=4096.
+
+One step = one hc_mix_fused call over one batch: x[4096, 20480] bf16 (168 MB,
+larger than the 129 MB L2, so no flush is needed between steps), W[24, 20480]
+fp32, hc_scale[3], hc_base[24], sinkhorn_iters 20 -> pre, post, comb.  Inputs
+are the seeded synthetic tensors of hcmix_inputs.
+
+Our arm prints one JSON line with:
+  value      device-timed us per call (CUDA events around K replays of a CUDA
+             graph holding one call; with N ranks, max elapsed / (K * N));
+  roofline   the contraction kernel timed alone with CUDA events on its stream,
+             algorithmic bytes (x once + W once) / average duration, against the
+             measured HBM copy bandwidth;
+  e2e        the same metric through the C ABI with host buffers: every step
+             copies x, W, hc_scale, hc_base from pinned host memory and reads
+             pre, post, comb back;
+  cpu_baseline  the CPU oracle on the same workload (rank 0, N = 1 only);
+  clocks     nvidia-smi samples taken during the timed region.
+`--impl reference` times the CPU oracle instead (bounded row samples per step).
+Multi-GPU (torchrun): each rank runs its own 4096 rows (weak scaling, rows are
+independent, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_ROWS = 4096
+K_COLS = 20480
+ITERS = 20
+RMS_EPS = 1e-6
+HC_EPS = 0.0
+METRIC = "µs/call and HBM GB/s (% of 8 TB/s roofline) for hc_mix_fused at M=4096"
+UNIT = "µs/call"
+WORKLOAD = f"hc_mix_fused M={M_ROWS} K={K_COLS} mix=24 hc=4 sinkhorn_iters={ITERS}"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--path", choices=("auto", "simt", "tc"), default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def rank_rows(rank: int, rows_per_rank: int = M_ROWS) -> int:
+    """First row of rank `rank`'s batch in the seed-0 activation stream."""
+    return rank * rows_per_rank
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "hyper_connection_mix_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profiled_traffic(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    from the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_sha") != source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", str(self.interval)],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]),
+                                 [p == "Active" for p in parts[5:9]]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        reasons = sorted({REASONS[i] for r in loaded for i, a in enumerate(r[3]) if a})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_time(x, W, sc, bs, rows: int, threads: int):
+    """Seconds for one oracle call on the first `rows` rows (all host threads)."""
+    import numpy as np
+    import oracle
+    xs = np.ascontiguousarray(x[:rows])
+    t0 = time.perf_counter()
+    oracle.fused(xs, W, sc, bs, ITERS, RMS_EPS, HC_EPS, threads=threads)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step one oracle call on a bounded
+    row sample, scaled to the 4096-row call; rank 0 only."""
+    if rank != 0:
+        return
+    import hcmix_inputs as hi
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    x = hi.make_x(M_ROWS)
+    W, sc, bs = hi.make_w(), hi.make_scale(), hi.make_base()
+    cal = max(cores, 64)
+    t_cal = cpu_oracle_time(x, W, sc, bs, cal, cores)
+    per_row = t_cal / cal
+    budget_s = 150.0
+    rows = int(max(1, min(M_ROWS, budget_s / max(1, args.steps + args.warmup) / per_row)))
+    for _ in range(args.warmup):
+        cpu_oracle_time(x, W, sc, bs, rows, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_oracle_time(x, W, sc, bs, rows, cores)
+    el = time.perf_counter() - t0
+    us_call = el / args.steps * (M_ROWS / rows) * 1e6
+    from hyper_connection_mix_gb300 import traffic
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us_call, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_ROWS, "K": K_COLS,
+                   "sample_rows_per_step": rows},
+        "hbm_gbs": traffic.algorithmic_bytes(M_ROWS, K_COLS) / (us_call * 1e-6) / 1e9,
+        "cpu_baseline": {"value": us_call, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} of {M_ROWS} rows per step, scaled to {M_ROWS}"},
+        "e2e": {"value": us_call, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import hcmix_inputs as hi
+    from hyper_connection_mix_gb300 import binding, traffic
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    M, K = M_ROWS, K_COLS
+    x_h = hi.make_x(M, row0=rank_rows(rank))
+    W_h, sc_h, bs_h = hi.make_w(), hi.make_scale(), hi.make_base()
+    x = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).to(device)
+    W, sc, bs = (torch.from_numpy(a).to(device) for a in (W_h, sc_h, bs_h))
+    ws = binding.alloc_workspace(M, K, device)
+    out = (torch.empty(M, 4, device=device), torch.empty(M, 4, device=device),
+           torch.empty(M, 4, 4, device=device))
+    path = args.path if args.path != "auto" else binding.hc_mix_auto_path(M)
+    stream = torch.cuda.Stream(device)
+
+    def call(s=stream, xx=x, WW=W, ss=sc, bb=bs, oo=out):
+        binding.hc_mix_fused(xx, WW, ss, bb, ITERS, RMS_EPS, HC_EPS, out=oo, workspace=ws,
+                             stream=s, path=path)
+
+    with torch.cuda.stream(stream):
+        call()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+    launches_per_call = 2 if path == "simt" else 3
+
+    # ---- device-timed value: K graph replays
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graph.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1), world, device)
+    ms_per_step = ms / args.steps
+    us_call = ms * 1e3 / (args.steps * world)
+    alg_bytes = traffic.algorithmic_bytes(M, K)
+
+    # ---- dominant kernel alone: the contraction, timed on its own stream
+    n_k = max(3, min(args.steps, 2000))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            binding.hc_mix_contract(x, W, ws, stream=stream, path=path)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(n_k):
+            binding.hc_mix_contract(x, W, ws, stream=stream, path=path)
+        c1.record(stream)
+        c1.synchronize()
+    k_us = c0.elapsed_time(c1) * 1e3 / n_k
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (k_us * 1e-6) / 1e9
+    kernel_name = "hcmix_simt_slice_kernel" if path == "simt" else "hcmix_tc_kernel"
+
+    # ---- end to end through the C ABI with host buffers
+    x_pin = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    W_pin, sc_pin, bs_pin = (torch.from_numpy(a).pin_memory() for a in (W_h, sc_h, bs_h))
+    out_pin = tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in out)
+    xd, Wd, scd, bsd = (torch.empty_like(t, device=device) for t in (x_pin, W_pin, sc_pin, bs_pin))
+    h2d = sum(t.numel() * t.element_size() for t in (x_pin, W_pin, sc_pin, bs_pin))
+    d2h = sum(t.numel() * t.element_size() for t in out_pin)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for d, h in ((xd, x_pin), (Wd, W_pin), (scd, sc_pin), (bsd, bs_pin)):
+                d.copy_(h, non_blocking=True)
+            call(stream, xd, Wd, scd, bsd, out)
+            for h, d in zip(out_pin, out):
+                h.copy_(d, non_blocking=True)
+    n_e2e = max(3, min(args.steps, 100))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    t1.record(stream)
+    t1.synchronize()
+    e2e_ms = reduce_max(t0.elapsed_time(t1), world, device)
+    e2e_us = e2e_ms * 1e3 / (n_e2e * world)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cores = host_cores()
+        t = cpu_oracle_time(x_h, W_h, sc_h, bs_h, M, cores)
+        reps = 1
+        if t * cores < 10.0:
+            reps = 2
+            t = (t + cpu_oracle_time(x_h, W_h, sc_h, bs_h, M, cores)) / 2
+        cpu = {"value": t * 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"full {M}-row call, mean of {reps}"}
+
+    line = {
+        "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "path": path, "cuda_graph": True,
+                   "l2": "inputs larger than L2: x is 168 MB per call (L2 129 MB), no flush",
+                   "inputs": "x bf16 N(0,1) seed 0 (rank r: rows 4096r..), W fp32 std K^-1/2"},
+        "hbm_gbs": alg_bytes / (us_call * 1e-6) / 1e9,
+        "roofline_pct_of_8tbs": alg_bytes / (us_call * 1e-6) / 8e12 * 100,
+        "rows_per_s": M / (us_call * 1e-6),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": kernel_name, "kernel_us": k_us,
+                     "traffic": profiled_traffic(kernel_name),
+                     "algorithmic_bytes": alg_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * launches_per_call,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -112,12 +112,13 @@ def outlier_channels(K: int, seed: int = SEED_OUTLIER, frac: float = 0.01) -> np
 
 
 def make_x(M: int, K: int = K_DEFAULT, seed: int = SEED_X, outliers: bool = False,
-           row_block: int = 64, threads: int | None = None, out: np.ndarray | None = None
-           ) -> np.ndarray:
-    """x[M, K] as uint16 bf16 bit patterns (row-major, prefix-stable in M).
+           row_block: int = 64, threads: int | None = None, out: np.ndarray | None = None,
+           row0: int = 0) -> np.ndarray:
+    """Rows row0 .. row0+M-1 of x[., K] as uint16 bf16 bit patterns.
 
-    Row blocks are drawn on a thread pool; every element depends only on its
-    index, so the result does not depend on the block size or thread count.
+    Row-major and prefix-stable in M.  Row blocks are drawn on a thread pool;
+    every element depends only on its index, so the result does not depend on
+    the block size or thread count.
     """
     if out is None:
         out = np.empty((M, K), np.uint16)
@@ -125,7 +126,7 @@ def make_x(M: int, K: int = K_DEFAULT, seed: int = SEED_X, outliers: bool = Fals
 
     def block(r0):
         r1 = min(M, r0 + row_block)
-        z = normal(seed, r0 * K, (r1 - r0) * K).reshape(r1 - r0, K)
+        z = normal(seed, (row0 + r0) * K, (r1 - r0) * K).reshape(r1 - r0, K)
         if ch is not None:
             z[:, ch] *= 20.0
         out[r0:r1] = bf16_bits_from_f64(z).reshape(r1 - r0, K)

@@ -1,0 +1,264 @@
+// C ABI of libhcmix.so (declared in include/hcmix.h).
+//
+// Host side only: argument validation in the style of the hc_fused page's
+// `eligible` gate (2-D bf16 x with unit inner stride, fp32 W of 24 rows, K of
+// the slice grid, hc == 4), workspace layout, kernel dispatch and status
+// reporting.  Every step of the computation runs in the kernels included below.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "hcmix.h"
+#include "hcmix_common.cuh"
+#include "hcmix_reduce.cuh"
+#include "hcmix_simt.cuh"
+#include "hcmix_tc.cuh"
+
+namespace hcmix {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int64_t kMaxK = int64_t(1) << 24;
+constexpr int64_t kMaxM = (int64_t(1) << 31) - 1;
+// AUTO uses the CUDA-core split-K kernel up to this many rows and the
+// tensor-core kernel above it.
+constexpr int64_t kSimtMaxRows = kMaxM;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Workspace {
+  size_t err_off = 0;     // uint32 device error word (256-byte header)
+  size_t limbs_off = 0;   // bf16 W limbs [4][24][K] for the tensor-core path
+  size_t limbs_bytes = 0;
+  size_t part_off = 0;    // fp32 partials [slices][25][Mpad]
+  size_t part_bytes = 0;
+  size_t total = 0;
+  int64_t Mpad = 0;
+  int64_t n_slices = 0;
+};
+
+Workspace workspace_layout(int64_t M, int64_t K) {
+  Workspace w;
+  w.n_slices = K / kSlice;
+  w.Mpad = (M + 127) / 128 * 128;
+  w.err_off = 0;
+  w.limbs_off = kAlign;
+  w.limbs_bytes = align_up((size_t)4 * kMix * (size_t)K * 2, kAlign);
+  w.part_off = w.limbs_off + w.limbs_bytes;
+  w.part_bytes = align_up((size_t)w.n_slices * kPartStride * (size_t)w.Mpad * 4, kAlign);
+  w.total = w.part_off + w.part_bytes;
+  return w;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+hcmix_status check_shape(int64_t M, int64_t K, int mix) {
+  if (M < 0 || K <= 0) return HCMIX_ERR_INVALID_ARG;
+  if (mix != kMix) return HCMIX_ERR_UNSUPPORTED;
+  if (K % kSlice != 0 || K > kMaxK || M > kMaxM) return HCMIX_ERR_UNSUPPORTED;
+  return HCMIX_OK;
+}
+
+hcmix_status check_stats_args(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                              int64_t M, int64_t K, int mix, void* workspace,
+                              size_t workspace_bytes) {
+  hcmix_status st = check_shape(M, K, mix);
+  if (st != HCMIX_OK) return st;
+  if (M == 0) return HCMIX_OK;
+  if (x == nullptr || W == nullptr || workspace == nullptr) return HCMIX_ERR_INVALID_ARG;
+  if (x_stride < K || w_stride < K) return HCMIX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (x_stride * 2) % 16 != 0) return HCMIX_ERR_ALIGNMENT;
+  if (!aligned(W, 16) || (w_stride * 4) % 16 != 0) return HCMIX_ERR_ALIGNMENT;
+  if (!aligned(workspace, kAlign)) return HCMIX_ERR_ALIGNMENT;
+  if (workspace_bytes < workspace_layout(M, K).total) return HCMIX_ERR_WORKSPACE;
+  return HCMIX_OK;
+}
+
+hcmix_status check_epilogue_args(int64_t K, int hc, const float* hc_scale, const float* hc_base,
+                                 int iters, const float* pre, const float* post,
+                                 const float* comb) {
+  if (hc != kHc) return HCMIX_ERR_UNSUPPORTED;
+  if (K <= 0 || iters < 0) return HCMIX_ERR_INVALID_ARG;
+  if (hc_scale == nullptr || hc_base == nullptr || pre == nullptr || post == nullptr ||
+      comb == nullptr)
+    return HCMIX_ERR_INVALID_ARG;
+  return HCMIX_OK;
+}
+
+hcmix_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
+}
+
+hcmix_path resolve_path(hcmix_path path, int64_t M) {
+  if (path == HCMIX_PATH_AUTO) return M <= kSimtMaxRows ? HCMIX_PATH_SIMT : HCMIX_PATH_TC;
+  return path;
+}
+
+// Contraction into the workspace partials (one launch or two).
+hcmix_status launch_contraction(const void* x, int64_t x_stride, const float* W,
+                                int64_t w_stride, int64_t M, int64_t K, void* workspace,
+                                cudaStream_t stream, hcmix_path path) {
+  const Workspace ws = workspace_layout(M, K);
+  char* base = static_cast<char*>(workspace);
+  float* part = reinterpret_cast<float*>(base + ws.part_off);
+  path = resolve_path(path, M);
+  if (path == HCMIX_PATH_SIMT) {
+    dim3 grid((unsigned)((M + kSimtRows - 1) / kSimtRows), (unsigned)ws.n_slices);
+    hcmix_simt_slice_kernel<<<grid, kSimtThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(x), x_stride, W, w_stride, (int)M, (int)ws.Mpad, part);
+    return launch_status();
+  }
+  if (path == HCMIX_PATH_TC) {
+    return tc_launch(static_cast<const uint16_t*>(x), x_stride, W, w_stride, M, K,
+                     reinterpret_cast<uint16_t*>(base + ws.limbs_off), part, (int)ws.Mpad,
+                     reinterpret_cast<uint32_t*>(base + ws.err_off), stream);
+  }
+  return HCMIX_ERR_INVALID_ARG;
+}
+
+hcmix_status launch_reduce(int64_t M, int64_t K, void* workspace, const float* hc_scale,
+                           const float* hc_base, int iters, float rms_eps, float hc_eps,
+                           float* pre, float* post, float* comb, float* mix_out, float* sq_out,
+                           int do_epilogue, cudaStream_t stream) {
+  const Workspace ws = workspace_layout(M, K);
+  const float* part =
+      reinterpret_cast<const float*>(static_cast<const char*>(workspace) + ws.part_off);
+  const float inv_k = (float)(1.0 / (double)K);
+  dim3 grid((unsigned)((M + kReduceRows - 1) / kReduceRows));
+  hcmix_reduce_kernel<<<grid, kReduceThreads, 0, stream>>>(
+      part, (int)ws.n_slices, (int)ws.Mpad, (int)M, inv_k, hc_scale, hc_base, iters, rms_eps,
+      hc_eps, pre, post, comb, mix_out, sq_out, do_epilogue);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace hcmix
+
+using namespace hcmix;
+
+extern "C" {
+
+size_t hc_mix_workspace_bytes(int64_t M, int64_t K, int mix) {
+  if (check_shape(M, K, mix) != HCMIX_OK) return 0;
+  return workspace_layout(M, K).total;
+}
+
+hcmix_path hc_mix_auto_path(int64_t M) { return resolve_path(HCMIX_PATH_AUTO, M); }
+
+hcmix_status hc_mix_stats_ex(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                             int64_t M, int64_t K, int mix, float* mix_out, float* sq_out,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             hcmix_path path) {
+  hcmix_status st = check_stats_args(x, x_stride, W, w_stride, M, K, mix, workspace,
+                                     workspace_bytes);
+  if (st != HCMIX_OK) return st;
+  if (path != HCMIX_PATH_AUTO && path != HCMIX_PATH_SIMT && path != HCMIX_PATH_TC)
+    return HCMIX_ERR_INVALID_ARG;
+  if (M == 0) return HCMIX_OK;
+  if (mix_out == nullptr || sq_out == nullptr) return HCMIX_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launch_contraction(x, x_stride, W, w_stride, M, K, workspace, s, path);
+  if (st != HCMIX_OK) return st;
+  return launch_reduce(M, K, workspace, nullptr, nullptr, 0, 0.f, 0.f, nullptr, nullptr, nullptr,
+                       mix_out, sq_out, 0, s);
+}
+
+hcmix_status hc_mix_contract_ex(const void* x, int64_t x_stride, const float* W,
+                                int64_t w_stride, int64_t M, int64_t K, int mix,
+                                void* workspace, size_t workspace_bytes, void* stream,
+                                hcmix_path path) {
+  hcmix_status st = check_stats_args(x, x_stride, W, w_stride, M, K, mix, workspace,
+                                     workspace_bytes);
+  if (st != HCMIX_OK) return st;
+  if (path != HCMIX_PATH_AUTO && path != HCMIX_PATH_SIMT && path != HCMIX_PATH_TC)
+    return HCMIX_ERR_INVALID_ARG;
+  if (M == 0) return HCMIX_OK;
+  return launch_contraction(x, x_stride, W, w_stride, M, K, workspace,
+                            static_cast<cudaStream_t>(stream), path);
+}
+
+hcmix_status hc_mix_stats(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                          int64_t M, int64_t K, int mix, float* mix_out, float* sq_out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  return hc_mix_stats_ex(x, x_stride, W, w_stride, M, K, mix, mix_out, sq_out, workspace,
+                         workspace_bytes, stream, HCMIX_PATH_AUTO);
+}
+
+hcmix_status hc_mix_sinkhorn(const float* mix, const float* sq, int64_t M, int64_t K, int mixn,
+                             int hc, const float* hc_scale, const float* hc_base,
+                             int sinkhorn_iters, float rms_eps, float hc_eps, float* pre,
+                             float* post, float* comb, void* stream) {
+  if (M < 0) return HCMIX_ERR_INVALID_ARG;
+  if (mixn != kMix) return HCMIX_ERR_UNSUPPORTED;
+  hcmix_status st =
+      check_epilogue_args(K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
+  if (st != HCMIX_OK) return st;
+  if (M > kMaxM) return HCMIX_ERR_UNSUPPORTED;
+  if (M == 0) return HCMIX_OK;
+  if (mix == nullptr || sq == nullptr) return HCMIX_ERR_INVALID_ARG;
+  const float inv_k = (float)(1.0 / (double)K);
+  hcmix_epilogue_kernel<<<(unsigned)((M + 127) / 128), 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      mix, sq, (int)M, inv_k, hc_scale, hc_base, sinkhorn_iters, rms_eps, hc_eps, pre, post, comb);
+  return launch_status();
+}
+
+hcmix_status hc_mix_fused_ex(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                             int64_t M, int64_t K, int mix, int hc, const float* hc_scale,
+                             const float* hc_base, int sinkhorn_iters, float rms_eps,
+                             float hc_eps, float* pre, float* post, float* comb, float* mix_out,
+                             float* sq_out, void* workspace, size_t workspace_bytes, void* stream,
+                             hcmix_path path) {
+  hcmix_status st = check_stats_args(x, x_stride, W, w_stride, M, K, mix, workspace,
+                                     workspace_bytes);
+  if (st != HCMIX_OK) return st;
+  st = check_epilogue_args(K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
+  if (st != HCMIX_OK) return st;
+  if (path != HCMIX_PATH_AUTO && path != HCMIX_PATH_SIMT && path != HCMIX_PATH_TC)
+    return HCMIX_ERR_INVALID_ARG;
+  if (M == 0) return HCMIX_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launch_contraction(x, x_stride, W, w_stride, M, K, workspace, s, path);
+  if (st != HCMIX_OK) return st;
+  return launch_reduce(M, K, workspace, hc_scale, hc_base, sinkhorn_iters, rms_eps, hc_eps, pre,
+                       post, comb, mix_out, sq_out, 1, s);
+}
+
+hcmix_status hc_mix_fused(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                          int64_t M, int64_t K, int mix, int hc, const float* hc_scale,
+                          const float* hc_base, int sinkhorn_iters, float rms_eps, float hc_eps,
+                          float* pre, float* post, float* comb, float* mix_out, float* sq_out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  return hc_mix_fused_ex(x, x_stride, W, w_stride, M, K, mix, hc, hc_scale, hc_base,
+                         sinkhorn_iters, rms_eps, hc_eps, pre, post, comb, mix_out, sq_out,
+                         workspace, workspace_bytes, stream, HCMIX_PATH_AUTO);
+}
+
+hcmix_status hc_mix_device_status(void* workspace, void* stream) {
+  if (workspace == nullptr || !aligned(workspace, kAlign)) return HCMIX_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HCMIX_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HCMIX_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemset(workspace, 0, sizeof word) != cudaSuccess) return HCMIX_ERR_CUDA;
+    return HCMIX_ERR_DEVICE;
+  }
+  return HCMIX_OK;
+}
+
+const char* hc_mix_status_string(hcmix_status status) {
+  switch (status) {
+    case HCMIX_OK: return "HCMIX_OK";
+    case HCMIX_ERR_INVALID_ARG: return "HCMIX_ERR_INVALID_ARG: invalid argument";
+    case HCMIX_ERR_ALIGNMENT: return "HCMIX_ERR_ALIGNMENT: pointer or row pitch not aligned";
+    case HCMIX_ERR_UNSUPPORTED: return "HCMIX_ERR_UNSUPPORTED: shape not supported";
+    case HCMIX_ERR_WORKSPACE: return "HCMIX_ERR_WORKSPACE: workspace too small";
+    case HCMIX_ERR_CUDA: return "HCMIX_ERR_CUDA: CUDA runtime or launch error";
+    case HCMIX_ERR_DEVICE: return "HCMIX_ERR_DEVICE: a kernel recorded an error";
+  }
+  return "HCMIX: unknown status";
+}
+
+}  // extern "C"

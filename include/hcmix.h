@@ -1,0 +1,142 @@
+/*
+ * hcmix.h -- C ABI of libhcmix.so: hyper-connection mix statistics on sm_103a.
+ *
+ * The operation (hc_fused page, "launcher/docker-images/mia-tp4/adapter/hc_fused.py",
+ * module docstring and fused_mix_stats_sinkhorn): for every row m of a bf16
+ * activation x[M, K] and an fp32 weight W[mix, K] (mix = 24 = 2*hc + hc*hc, hc = 4)
+ *
+ *   mix[m, j] = sum over K of x[m, k] * W[j, k], with K walked in slices of 256
+ *               columns and each slice in four chunks of 64: every chunk's dot
+ *               product is rounded once to fp32, a slice total starts from zero
+ *               and adds its chunks in order, and the grand total starts from
+ *               zero and adds the slice totals in slice order;
+ *   sq[m]     = sum of x[m, k]^2 by the page's fixed tree inside every chunk
+ *               (_sq_tree), then the same chunk / slice / total order;
+ *   epilogue  : r = 1 / sqrt(sq * (1/K) + rms_eps);
+ *               logit[j] = mix[j] * r * hc_scale[g(j)] + hc_base[j],
+ *                 g = 0 for j < hc (pre), 1 for hc <= j < 2hc (post), 2 else (comb);
+ *               pre  = sigmoid(logit[0:hc]);  post = 2 * sigmoid(logit[hc:2hc]);
+ *               comb = sinkhorn_iters rounds of (divide each row by its sum + hc_eps,
+ *                      then each column by its sum + hc_eps) of exp(logit[2hc:]),
+ *                      viewed row-major as hc x hc.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing, keeps no global state and never synchronises the host.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream), so calls may be captured in a CUDA graph.
+ *   - Layouts are row-major.  x rows are `x_stride` elements apart (inner stride
+ *     1); W rows are `w_stride` elements apart (inner stride 1).
+ *   - Arguments are validated on the host before any launch.  A failed check
+ *     returns an error status and launches nothing.  Launch failures return
+ *     HCMIX_ERR_CUDA.  Kernels never trap: a bounded wait that runs out sets a
+ *     device error word in the workspace, read with hc_mix_device_status().
+ *   - NaN / Inf inputs propagate per IEEE arithmetic without checks.
+ *   - Supported shapes: mix == 24, hc == 4, K a positive multiple of 256 up to
+ *     2^24, 0 <= M < 2^31.  Finite |x| < 2^112 and |W| < 2^112 (the exact
+ *     limb split of the contraction needs that headroom).
+ */
+#ifndef HCMIX_H
+#define HCMIX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HCMIX_OK = 0,
+  HCMIX_ERR_INVALID_ARG = 1, /* negative size, null pointer, stride < K, iters < 0 */
+  HCMIX_ERR_ALIGNMENT = 2,   /* x, W or workspace misaligned, or row pitch not 16-byte */
+  HCMIX_ERR_UNSUPPORTED = 3, /* mix != 24, hc != 4, K not a multiple of 256, too large */
+  HCMIX_ERR_WORKSPACE = 4,   /* workspace smaller than hc_mix_workspace_bytes() */
+  HCMIX_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  HCMIX_ERR_DEVICE = 6       /* a kernel recorded an error (see hc_mix_device_status) */
+} hcmix_status;
+
+/* Which contraction kernel runs.  AUTO picks by M; the others force one path
+ * (both give results within the stated tolerance of each other). */
+typedef enum {
+  HCMIX_PATH_AUTO = 0,
+  HCMIX_PATH_SIMT = 1,  /* CUDA-core split-K kernel (small M) */
+  HCMIX_PATH_TC = 2     /* tcgen05 tensor-core kernel (large M) */
+} hcmix_path;
+
+/* Bytes of device workspace that hc_mix_stats / hc_mix_fused need for M rows.
+ * The workspace must be 256-byte aligned and zeroed once before its first use
+ * (its first 256 bytes hold the device error word); after that every call
+ * writes what it reads, so no per-call clearing is needed.  A workspace sized
+ * for M rows serves any smaller M.  Returns 0 for unsupported (K, mix). */
+size_t hc_mix_workspace_bytes(int64_t M, int64_t K, int mix);
+
+/* mix_out[M, mix] (fp32) and sq_out[M] (fp32): the contraction and the sum of
+ * squares in the slice order above.
+ *   x        bf16 [M, x_stride], 16-byte aligned, x_stride % 8 == 0, x_stride >= K
+ *   W        fp32 [mix, w_stride], 16-byte aligned, w_stride % 4 == 0, w_stride >= K
+ *   mix_out  fp32 [M, mix] (contiguous), sq_out fp32 [M]
+ *   workspace / workspace_bytes: device scratch, see hc_mix_workspace_bytes. */
+hcmix_status hc_mix_stats(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                          int64_t M, int64_t K, int mix, float* mix_out, float* sq_out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* The epilogue alone, from mix[M, mix] and sq[M] (fp32, device, contiguous):
+ * writes pre[M, hc], post[M, hc], comb[M, hc, hc] (fp32, contiguous).
+ * hc_scale: fp32[3] device; hc_base: fp32[mix] device.  K only sets 1/K. */
+hcmix_status hc_mix_sinkhorn(const float* mix, const float* sq, int64_t M, int64_t K, int mixn,
+                             int hc, const float* hc_scale, const float* hc_base,
+                             int sinkhorn_iters, float rms_eps, float hc_eps,
+                             float* pre, float* post, float* comb, void* stream);
+
+/* The whole path: contraction, sum of squares and epilogue.  mix_out / sq_out
+ * may be NULL; when given they receive the intermediate statistics. */
+hcmix_status hc_mix_fused(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                          int64_t M, int64_t K, int mix, int hc,
+                          const float* hc_scale, const float* hc_base, int sinkhorn_iters,
+                          float rms_eps, float hc_eps,
+                          float* pre, float* post, float* comb,
+                          float* mix_out, float* sq_out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* As hc_mix_stats / hc_mix_fused with an explicit kernel path (for tests and
+ * benchmarks); HCMIX_PATH_AUTO gives the plain entry points' choice. */
+hcmix_status hc_mix_stats_ex(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                             int64_t M, int64_t K, int mix, float* mix_out, float* sq_out,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             hcmix_path path);
+hcmix_status hc_mix_fused_ex(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                             int64_t M, int64_t K, int mix, int hc,
+                             const float* hc_scale, const float* hc_base, int sinkhorn_iters,
+                             float rms_eps, float hc_eps,
+                             float* pre, float* post, float* comb,
+                             float* mix_out, float* sq_out,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             hcmix_path path);
+
+/* The contraction phase alone (the dominant kernel of hc_mix_stats and
+ * hc_mix_fused): writes the per-slice partial totals into the workspace and
+ * nothing else.  Arguments as hc_mix_stats_ex.  For timing and profiling the
+ * phase on its own stream position; the partials are not a public format. */
+hcmix_status hc_mix_contract_ex(const void* x, int64_t x_stride, const float* W,
+                                int64_t w_stride, int64_t M, int64_t K, int mix,
+                                void* workspace, size_t workspace_bytes, void* stream,
+                                hcmix_path path);
+
+/* The path HCMIX_PATH_AUTO takes for M rows. */
+hcmix_path hc_mix_auto_path(int64_t M);
+
+/* Synchronises `stream`, then reads and clears the device error word that
+ * kernels set in `workspace` when a bounded wait runs out.  HCMIX_OK when clean,
+ * HCMIX_ERR_DEVICE when a kernel recorded an error, HCMIX_ERR_CUDA when the
+ * stream reports a CUDA error. */
+hcmix_status hc_mix_device_status(void* workspace, void* stream);
+
+/* Static, human-readable name of a status. */
+const char* hc_mix_status_string(hcmix_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HCMIX_H */

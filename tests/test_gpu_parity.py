@@ -1,0 +1,263 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Tolerances (task statement): mix within max(2e-6 |o|, 1e-6); pre, post and comb
+within 1e-5 absolute.  sq is compared bit for bit: the kernels evaluate the
+page's fixed tree on exact squares with the same round-to-nearest adds.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import hcmix_inputs as hi
+import oracle
+from hyper_connection_mix_gb300 import binding
+
+pytestmark = pytest.mark.gpu
+
+THREADS = os.cpu_count() or 1
+PATHS = ("simt", "tc")
+
+
+def dev_x(x):
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def path_available(path):
+    x = torch.zeros(1, 256, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(24, 256, dtype=torch.float32, device="cuda")
+    try:
+        binding.hc_mix_stats(x, W, path=path)
+        return True
+    except binding.HcMixError as e:
+        if e.status == 3:
+            return False
+        raise
+
+
+@pytest.fixture(scope="module", params=PATHS)
+def path(request):
+    if not path_available(request.param):
+        pytest.fail(f"kernel path {request.param} is not available in this library")
+    return request.param
+
+
+def run(x, W, sc, bs, path, iters=20, rms_eps=1e-6, hc_eps=0.0, x_dev=None):
+    xt = dev_x(x) if x_dev is None else x_dev
+    out = binding.hc_mix_fused(xt, dev(W), dev(sc), dev(bs), iters, rms_eps, hc_eps,
+                               want_stats=True, path=path)
+    torch.cuda.synchronize()
+    return [o.cpu().numpy() for o in out]
+
+
+def assert_mix_close(g, o, what=""):
+    thr = np.maximum(2e-6 * np.abs(o.astype(np.float64)), 1e-6)
+    d = np.abs(g.astype(np.float64) - o)
+    bad = d > thr
+    assert not bad.any(), (f"{what} mix: {bad.sum()} of {bad.size} outside tolerance, "
+                           f"max ratio {(d / thr).max():.3f}")
+    return float((d / thr).max())
+
+
+def assert_epilogue_close(got, want, what=""):
+    for name, g, o in zip(("pre", "post", "comb"), got, want):
+        err = float(np.max(np.abs(g.astype(np.float64) - o))) if g.size else 0.0
+        assert err <= 1e-5, f"{what} {name}: max abs error {err}"
+
+
+def check_all(x, W, sc, bs, path, what, **kw):
+    want = oracle.fused(x, W, sc, bs, threads=THREADS, **kw)
+    got = run(x, W, sc, bs, path, **kw)
+    assert_epilogue_close(got[:3], want[:3], what)
+    r = assert_mix_close(got[3], want[3], what)
+    assert np.array_equal(got[4], want[4]), f"{what} sq not bit-identical"
+    return r
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 7, 8])
+@pytest.mark.parametrize("K", [256, 512, 1024])
+def test_tiny(path, M, K):
+    x = hi.make_x(M, K=K)
+    check_all(x, hi.make_w(K=K), hi.make_scale(), hi.make_base(), path, f"M={M} K={K}")
+
+
+@pytest.mark.parametrize("M", [33, 100, 129, 255, 300])
+def test_ragged_rows_several_tiles(path, M):
+    K = 2048
+    check_all(hi.make_x(M, K=K), hi.make_w(K=K), hi.make_scale(), hi.make_base(), path,
+              f"M={M}")
+
+
+def test_config_m16(path):
+    check_all(hi.make_x(16), hi.make_w(), hi.make_scale(), hi.make_base(), path, "M=16")
+
+
+def test_config_m512_outliers(path):
+    check_all(hi.make_x(512, outliers=True), hi.make_w(), hi.make_scale(), hi.make_base(), path,
+              "M=512 outliers")
+
+
+def test_config_decode_sweep(path):
+    x = hi.make_x(256)
+    W, sc, bs = hi.make_w(), hi.make_scale(), hi.make_base()
+    for M in (1, 4, 16, 64, 128, 256):
+        check_all(np.ascontiguousarray(x[:M]), W, sc, bs, path, f"sweep M={M}")
+
+
+def test_config_m4096_full(path):
+    ratio = check_all(hi.make_x(4096), hi.make_w(), hi.make_scale(), hi.make_base(), path,
+                      "M=4096")
+    print(f"M=4096 {path}: max mix error / tolerance = {ratio:.3f}")
+
+
+def test_integer_inputs_bit_exact(path):
+    """x in {-4..4}, W in {-8..8}: every partial sum is an integer < 2**24, so
+    every correct evaluation order gives the exact integer product."""
+    rng = np.random.default_rng(5)
+    K = 2048
+    xi = rng.integers(-4, 5, size=(130, K))
+    wi = rng.integers(-8, 9, size=(24, K))
+    got = run(hi.bf16_bits_from_f64(xi), wi.astype(np.float32), hi.make_scale(),
+              hi.make_base(), path)
+    assert np.array_equal(got[3].astype(np.int64), xi @ wi.T)
+    assert np.array_equal(got[4].astype(np.int64), (xi * xi).sum(1))
+
+
+def test_one_hot_rows_select_columns(path):
+    K = 1024
+    W = (np.random.default_rng(3).standard_normal((24, K)) * 0.01).astype(np.float32)
+    cols = [0, 1, 63, 64, 255, 256, 511, 1023]
+    x = np.zeros((len(cols), K))
+    for r, k in enumerate(cols):
+        x[r, k] = 1.0
+    got = run(hi.bf16_bits_from_f64(x), W, hi.make_scale(), hi.make_base(), path)
+    for r, k in enumerate(cols):
+        assert np.array_equal(got[3][r], W[:, k])
+
+
+def test_strided_inputs(path):
+    K, M = 1024, 70
+    rng = np.random.default_rng(8)
+    xs = hi.bf16_bits_from_f64(rng.standard_normal((M, K + 64)))
+    Wf = (rng.standard_normal((24, K + 32)) * 0.03).astype(np.float32)
+    sc, bs = hi.make_scale(), hi.make_base()
+    want = oracle.fused(np.ascontiguousarray(xs[:, :K]), np.ascontiguousarray(Wf[:, :K]), sc, bs)
+    xt = dev_x(xs)[:, :K]
+    Wt = dev(Wf)[:, :K]
+    out = binding.hc_mix_fused(xt, Wt, dev(sc), dev(bs), want_stats=True, path=path)
+    torch.cuda.synchronize()
+    got = [o.cpu().numpy() for o in out]
+    assert_epilogue_close(got[:3], want[:3], "strided")
+    assert_mix_close(got[3], want[3], "strided")
+    assert np.array_equal(got[4], want[4])
+
+
+def test_deterministic_repeat(path):
+    x, W, sc, bs = hi.make_x(300), hi.make_w(), hi.make_scale(), hi.make_base()
+    xt = dev_x(x)
+    a = run(x, W, sc, bs, path, x_dev=xt)
+    b = run(x, W, sc, bs, path, x_dev=xt)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def test_stats_and_sinkhorn_entry_points_agree_with_fused(path):
+    x, W, sc, bs = hi.make_x(77), hi.make_w(), hi.make_scale(), hi.make_base()
+    xt, Wt, sct, bst = dev_x(x), dev(W), dev(sc), dev(bs)
+    pre, post, comb, mix, sq = binding.hc_mix_fused(xt, Wt, sct, bst, want_stats=True, path=path)
+    mix2, sq2 = binding.hc_mix_stats(xt, Wt, path=path)
+    pre2, post2, comb2 = binding.hc_mix_sinkhorn(mix2, sq2, x.shape[1], sct, bst)
+    torch.cuda.synchronize()
+    for a, b in ((mix, mix2), (sq, sq2), (pre, pre2), (post, post2), (comb, comb2)):
+        assert torch.equal(a, b)
+
+
+def test_zero_weights_and_zero_rows(path):
+    K = 512
+    x = hi.make_x(9, K=K)
+    x[3] = 0
+    got = run(x, np.zeros((24, K), np.float32), hi.make_scale(), np.zeros(24, np.float32), path)
+    assert np.all(got[0] == 0.5) and np.all(got[1] == 1.0) and np.all(got[2] == 0.25)
+    assert got[4][3] == 0
+
+
+def test_sinkhorn_iteration_counts(path):
+    x, W, sc, bs = hi.make_x(20, K=1024), hi.make_w(K=1024), hi.make_scale(), hi.make_base()
+    for iters in (0, 1, 3, 50):
+        check_all(x, W, sc, bs, path, f"iters={iters}", iters=iters)
+    check_all(x, W, sc, bs, path, "hc_eps", hc_eps=0.01)
+
+
+def test_empty_batch_is_a_no_op(path):
+    x = torch.zeros(0, 256, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(24, 256, dtype=torch.float32, device="cuda")
+    s = torch.ones(3, device="cuda"); b = torch.zeros(24, device="cuda")
+    out = binding.hc_mix_fused(x, W, s, b, path=path)
+    assert all(o.shape[0] == 0 for o in out)
+
+
+def test_device_status_clean_after_runs(path):
+    x, W = hi.make_x(200), hi.make_w()
+    ws = binding.alloc_workspace(200, x.shape[1])
+    binding.hc_mix_fused(dev_x(x), dev(W), dev(hi.make_scale()), dev(hi.make_base()),
+                         workspace=ws, path=path)
+    assert binding.hc_mix_device_status(ws) == 0
+
+
+def test_paths_agree_on_overlapping_sizes():
+    if not (path_available("simt") and path_available("tc")):
+        pytest.fail("both kernel paths must be available")
+    x, W, sc, bs = hi.make_x(256), hi.make_w(), hi.make_scale(), hi.make_base()
+    a = run(x, W, sc, bs, "simt")
+    b = run(x, W, sc, bs, "tc")
+    assert np.array_equal(a[4], b[4])
+    assert_mix_close(b[3], a[3].astype(np.float64), "simt vs tc")
+    for u, v in zip(a[:3], b[:3]):
+        assert np.max(np.abs(u - v)) <= 1e-5
+
+
+def test_stack86_m16384_sampled():
+    """The 43-layer stack: 86 calls at M=16384 with distinct W / scale / base,
+    captured once in a CUDA graph as the benchmark runs it.  Sampled rows of every
+    call are checked element by element; every row is checked for the
+    properties that hold at any size."""
+    M, K, calls = 16384, 20480, 86
+    x = hi.make_x(M)
+    xt = dev_x(x)
+    params = []
+    for i in range(calls):
+        sw, ss, sb = hi.layer_seeds(i)
+        params.append((hi.make_w(seed=sw), hi.make_scale(seed=ss), hi.make_base(seed=sb)))
+    dparams = [(dev(W), dev(s), dev(b)) for W, s, b in params]
+    ws = binding.alloc_workspace(M, K)
+    outs = [(torch.empty(M, 4, device="cuda"), torch.empty(M, 4, device="cuda"),
+             torch.empty(M, 4, 4, device="cuda"), torch.empty(M, 24, device="cuda"),
+             torch.empty(M, device="cuda")) for _ in range(calls)]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        binding.hc_mix_fused(xt, *dparams[0], out=outs[0], workspace=ws)  # warm-up
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(calls):
+                binding.hc_mix_fused(xt, *dparams[i], out=outs[i], workspace=ws)
+        g.replay()
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.arange(0, M, 331), [M - 1]]))
+    xs = np.ascontiguousarray(x[rows])
+    for i in range(calls):
+        W, s, b = params[i]
+        want = oracle.fused(xs, W, s, b, threads=THREADS)
+        got = [o.cpu().numpy() for o in outs[i]]
+        assert_epilogue_close([got[0][rows], got[1][rows], got[2][rows]], want[:3], f"call {i}")
+        assert_mix_close(got[3][rows], want[3], f"call {i}")
+        assert np.array_equal(got[4][rows], want[4])
+        pre, post, comb = got[:3]
+        assert np.all((pre > 0) & (pre < 1)) and np.all((post > 0) & (post < 2))
+        assert np.all(comb > 0)
+        assert np.max(np.abs(comb.sum(1) - 1)) < 1e-5
+    assert binding.hc_mix_device_status(ws) == 0
