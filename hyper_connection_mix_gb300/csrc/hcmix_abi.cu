@@ -75,13 +75,15 @@ hcmix_status check_stats_args(const void* x, int64_t x_stride, const float* W, i
   return HCMIX_OK;
 }
 
-hcmix_status check_epilogue_args(int64_t K, int hc, const float* hc_scale, const float* hc_base,
-                                 int iters, const float* pre, const float* post,
-                                 const float* comb) {
+// Value checks of the epilogue arguments; pointers are checked only when there
+// is at least one row (empty tensors may carry null data pointers).
+hcmix_status check_epilogue_args(int64_t M, int64_t K, int hc, const float* hc_scale,
+                                 const float* hc_base, int iters, const float* pre,
+                                 const float* post, const float* comb) {
   if (hc != kHc) return HCMIX_ERR_UNSUPPORTED;
   if (K <= 0 || iters < 0) return HCMIX_ERR_INVALID_ARG;
-  if (hc_scale == nullptr || hc_base == nullptr || pre == nullptr || post == nullptr ||
-      comb == nullptr)
+  if (M > 0 && (hc_scale == nullptr || hc_base == nullptr || pre == nullptr ||
+                post == nullptr || comb == nullptr))
     return HCMIX_ERR_INVALID_ARG;
   return HCMIX_OK;
 }
@@ -192,7 +194,7 @@ hcmix_status hc_mix_sinkhorn(const float* mix, const float* sq, int64_t M, int64
   if (M < 0) return HCMIX_ERR_INVALID_ARG;
   if (mixn != kMix) return HCMIX_ERR_UNSUPPORTED;
   hcmix_status st =
-      check_epilogue_args(K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
+      check_epilogue_args(M, K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
   if (st != HCMIX_OK) return st;
   if (M > kMaxM) return HCMIX_ERR_UNSUPPORTED;
   if (M == 0) return HCMIX_OK;
@@ -212,7 +214,7 @@ hcmix_status hc_mix_fused_ex(const void* x, int64_t x_stride, const float* W, in
   hcmix_status st = check_stats_args(x, x_stride, W, w_stride, M, K, mix, workspace,
                                      workspace_bytes);
   if (st != HCMIX_OK) return st;
-  st = check_epilogue_args(K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
+  st = check_epilogue_args(M, K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
   if (st != HCMIX_OK) return st;
   if (path != HCMIX_PATH_AUTO && path != HCMIX_PATH_SIMT && path != HCMIX_PATH_TC)
     return HCMIX_ERR_INVALID_ARG;

@@ -91,12 +91,14 @@ def test_fused_and_sinkhorn_validation(L):
     assert fused(sc=None) == 1
     assert fused(comb=None) == 1
     assert fused(M=0, x=None) == 0
+    assert fused(M=0, x=None, pre=None, post=None, comb=None) == 0  # empty outputs
     s = L.hc_mix_sinkhorn
     assert s(P, P, 4, 1024, 24, 4, P, P, -1, 1e-6, 0.0, P, P, P, None) == 1
     assert s(P, P, 4, 1024, 16, 4, P, P, 20, 1e-6, 0.0, P, P, P, None) == 3
     assert s(P, P, -4, 1024, 24, 4, P, P, 20, 1e-6, 0.0, P, P, P, None) == 1
     assert s(None, P, 4, 1024, 24, 4, P, P, 20, 1e-6, 0.0, P, P, P, None) == 1
     assert s(None, None, 0, 1024, 24, 4, P, P, 20, 1e-6, 0.0, P, P, P, None) == 0
+    assert s(None, None, 0, 1024, 24, 4, None, None, 20, 1e-6, 0.0, None, None, None, None) == 0
 
 
 def test_device_status_rejects_bad_workspace(L):
