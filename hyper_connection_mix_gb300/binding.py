@@ -28,7 +28,7 @@ PATHS = {"auto": 0, "simt": 1, "tc": 2}
 # every symbol include/hcmix.h declares
 EXPORTS = ("hc_mix_workspace_bytes", "hc_mix_stats", "hc_mix_sinkhorn", "hc_mix_fused",
            "hc_mix_stats_ex", "hc_mix_fused_ex", "hc_mix_contract_ex", "hc_mix_auto_path",
-           "hc_mix_device_status", "hc_mix_status_string")
+           "hc_mix_device_status", "hc_mix_status_string", "hc_mix_fused_noalloc")
 
 
 class HcMixError(RuntimeError):
@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
             L.hc_mix_fused_ex.argtypes = fused_args + [I]
             L.hc_mix_contract_ex.restype = I
             L.hc_mix_contract_ex.argtypes = [P, I64, P, I64, I64, I64, I, P, S, P, I]
+            L.hc_mix_fused_noalloc.restype = I
+            L.hc_mix_fused_noalloc.argtypes = [P, I64, P, I64, I64, I64, I, I, P, P, I, F, F,
+                                               P, P, P, P, P, P]
             L.hc_mix_auto_path.restype = I
             L.hc_mix_auto_path.argtypes = [I64]
             L.hc_mix_device_status.restype = I

@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "hcmix.h"
 #include "hcmix_common.cuh"
@@ -234,6 +235,81 @@ hcmix_status hc_mix_fused(const void* x, int64_t x_stride, const float* W, int64
   return hc_mix_fused_ex(x, x_stride, W, w_stride, M, K, mix, hc, hc_scale, hc_base,
                          sinkhorn_iters, rms_eps, hc_eps, pre, post, comb, mix_out, sq_out,
                          workspace, workspace_bytes, stream, HCMIX_PATH_AUTO);
+}
+
+// ---- hc_mix_fused_noalloc: the split-K path with its partials in a fixed
+// device array instead of a caller workspace, for callers that may not
+// allocate device memory.  The array lives in this file; host code only ever
+// uses the device address looked up below, never the array's host-side name.
+}  // extern "C"
+
+namespace hcmix {
+namespace {
+
+constexpr size_t kStaticScratchBytes = HC_MIX_STATIC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_scratch_mutex;
+void* g_static_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+hcmix_status static_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return HCMIX_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
+  if (g_static_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+      return HCMIX_ERR_CUDA;
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return HCMIX_OK;
+}
+
+}  // namespace
+}  // namespace hcmix
+
+extern "C" {
+
+hcmix_status hc_mix_fused_noalloc(const void* x, int64_t x_stride, const float* W,
+                                  int64_t w_stride, int64_t M, int64_t K, int mix, int hc,
+                                  const float* hc_scale, const float* hc_base,
+                                  int sinkhorn_iters, float rms_eps, float hc_eps, float* pre,
+                                  float* post, float* comb, float* mix_out, float* sq_out,
+                                  void* stream) {
+  hcmix_status st = check_shape(M, K, mix);
+  if (st != HCMIX_OK) return st;
+  st = check_epilogue_args(M, K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
+  if (st != HCMIX_OK) return st;
+  if (M == 0) return HCMIX_OK;
+  if (x == nullptr || W == nullptr) return HCMIX_ERR_INVALID_ARG;
+  if (x_stride < K || w_stride < K) return HCMIX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (x_stride * 2) % 16 != 0) return HCMIX_ERR_ALIGNMENT;
+  if (!aligned(W, 16) || (w_stride * 4) % 16 != 0) return HCMIX_ERR_ALIGNMENT;
+  const int64_t n_slices = K / kSlice;
+  const int64_t Mpad = (M + 127) / 128 * 128;
+  const size_t need = (size_t)n_slices * kPartStride * (size_t)Mpad * 4;
+  if (need > kStaticScratchBytes) return HCMIX_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  st = static_scratch_address(&scratch);
+  if (st != HCMIX_OK) return st;
+  float* part = static_cast<float*>(scratch);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dim3 grid((unsigned)((M + kSimtRows - 1) / kSimtRows), (unsigned)n_slices);
+  hcmix_simt_slice_kernel<<<grid, kSimtThreads, 0, s>>>(
+      static_cast<const uint16_t*>(x), x_stride, W, w_stride, (int)M, (int)Mpad, part);
+  st = launch_status();
+  if (st != HCMIX_OK) return st;
+  const float inv_k = (float)(1.0 / (double)K);
+  hcmix_reduce_kernel<<<(unsigned)((M + kReduceRows - 1) / kReduceRows), kReduceThreads, 0, s>>>(
+      part, (int)n_slices, (int)Mpad, (int)M, inv_k, hc_scale, hc_base, sinkhorn_iters, rms_eps,
+      hc_eps, pre, post, comb, mix_out, sq_out, 1);
+  return launch_status();
 }
 
 hcmix_status hc_mix_device_status(void* workspace, void* stream) {

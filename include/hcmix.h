@@ -22,7 +22,9 @@
  *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
- *     allocates nothing, keeps no global state and never synchronises the host.
+ *     allocates nothing and never synchronises the host.  Its only global state
+ *     is the fixed scratch array of hc_mix_fused_noalloc and that array's cached
+ *     device addresses.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream), so calls may be captured in a CUDA graph.
  *   - Layouts are row-major.  x rows are `x_stride` elements apart (inner stride
@@ -125,6 +127,39 @@ hcmix_status hc_mix_contract_ex(const void* x, int64_t x_stride, const float* W,
 
 /* The path HCMIX_PATH_AUTO takes for M rows. */
 hcmix_path hc_mix_auto_path(int64_t M);
+
+/* hc_mix_fused without a workspace argument, for callers that cannot hand the
+ * library any device memory of their own: for example an engine that reserves
+ * its whole device memory budget at start-up and forbids any later
+ * cudaMalloc (a late allocation can fail, fragment its pool or synchronise
+ * the device), or a plug-in living inside a host framework that owns every
+ * device allocation.  The hc_fused page has no counterpart; this is a
+ * convenience of this library.
+ *
+ * Instead of a caller workspace it uses a fixed scratch array of
+ * HC_MIX_STATIC_SCRATCH_BYTES (2 MiB) that the library defines in device
+ * memory; every GPU that loads libhcmix.so holds that array until the process
+ * exits.  It runs the CUDA-core split-K kernel (HCMIX_PATH_SIMT) and allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Limit: ceil(M / 128) * 128 * (K / 256) * 25 * 4 bytes must fit the
+ *     scratch, i.e. M <= 256 at K = 20480.  Larger problems return
+ *     HCMIX_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address once and keeps it for later calls; make that
+ *     first call before any stream capture starts on that device.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Every call writes all the scratch it reads, so nothing needs clearing,
+ *     but calls whose kernels overlap on the GPU (different streams, or
+ *     different host threads on the same device) race on the array: order
+ *     them on one stream or serialise them.
+ * Other arguments, outputs and error behaviour are those of hc_mix_fused. */
+#define HC_MIX_STATIC_SCRATCH_BYTES (2u << 20)
+hcmix_status hc_mix_fused_noalloc(const void* x, int64_t x_stride, const float* W,
+                                  int64_t w_stride, int64_t M, int64_t K, int mix, int hc,
+                                  const float* hc_scale, const float* hc_base,
+                                  int sinkhorn_iters, float rms_eps, float hc_eps,
+                                  float* pre, float* post, float* comb,
+                                  float* mix_out, float* sq_out, void* stream);
 
 /* Synchronises `stream`, then reads and clears the device error word that
  * kernels set in `workspace` when a bounded wait runs out.  HCMIX_OK when clean,

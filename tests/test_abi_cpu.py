@@ -99,6 +99,13 @@ def test_fused_and_sinkhorn_validation(L):
     assert s(None, P, 4, 1024, 24, 4, P, P, 20, 1e-6, 0.0, P, P, P, None) == 1
     assert s(None, None, 0, 1024, 24, 4, P, P, 20, 1e-6, 0.0, P, P, P, None) == 0
     assert s(None, None, 0, 1024, 24, 4, None, None, 20, 1e-6, 0.0, None, None, None, None) == 0
+    nf = L.hc_mix_fused_noalloc
+    assert nf(None, 256, None, 256, 0, 256, 24, 4, None, None, 20, 1e-6, 0.0,
+              None, None, None, None, None, None) == 0
+    assert nf(P, 1024, P, 1024, 257, 20480, 24, 4, P, P, 20, 1e-6, 0.0,
+              P, P, P, None, None, None) == 1        # stride < K
+    assert nf(P, 20480, P, 20480, 257, 20480, 24, 4, P, P, 20, 1e-6, 0.0,
+              P, P, P, None, None, None) == 4        # beyond the fixed scratch
 
 
 def test_device_status_rejects_bad_workspace(L):
