@@ -24,7 +24,7 @@ constexpr int64_t kMaxK = int64_t(1) << 24;
 constexpr int64_t kMaxM = (int64_t(1) << 31) - 1;
 // AUTO uses the CUDA-core split-K kernel up to this many rows and the
 // tensor-core kernel above it.
-constexpr int64_t kSimtMaxRows = kMaxM;
+constexpr int64_t kSimtMaxRows = 64;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

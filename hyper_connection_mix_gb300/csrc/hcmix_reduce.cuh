@@ -5,9 +5,10 @@
 // this kernel does the same from the workspace partials
 // part[(slice * 25 + j) * Mpad + row] (j < 24: mix, j = 24: sum of squares).
 //
-// Layout: 256 threads per CTA, 32 rows per CTA.  Warp w sums outputs
-// j = w, w + 8, w + 16 (and warp 0 also j = 24) for the 32 rows, one row per
-// lane, so every load of a (slice, j) pair is 32 consecutive floats.  Warp 0
+// Layout: 32 rows per CTA and one warp per output j (25 warps, one row per
+// lane), so every load of a (slice, j) pair is 32 consecutive floats.  Each
+// lane issues its slice loads in batches of 40 before adding them in slice
+// order, so the L2 latency is paid per batch rather than per slice.  Warp 0
 // then runs the epilogue, one row per lane.
 #pragma once
 
@@ -16,7 +17,8 @@
 namespace hcmix {
 
 constexpr int kReduceRows = 32;
-constexpr int kReduceThreads = 256;
+constexpr int kReduceThreads = 32 * kPartStride;
+constexpr int kReduceBatch = 40;
 
 __global__ void __launch_bounds__(kReduceThreads)
 hcmix_reduce_kernel(const float* __restrict__ part, int n_slices, int Mpad, int M, float inv_k,
@@ -25,20 +27,25 @@ hcmix_reduce_kernel(const float* __restrict__ part, int n_slices, int Mpad, int 
                     float* __restrict__ post, float* __restrict__ comb,
                     float* __restrict__ mix_out, float* __restrict__ sq_out, int do_epilogue) {
   __shared__ float s_tot[kPartStride][kReduceRows + 1];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, out = threadIdx.x >> 5;  // out: mix index or 24 (sq)
   const int row = blockIdx.x * kReduceRows + lane;
-  for (int j = warp; j < kPartStride; j += kReduceThreads / 32) {
-    float t = 0.0f;
-    if (row < M) {
-      const float* p = part + (int64_t)j * Mpad + row;
-      const int64_t step = (int64_t)kPartStride * Mpad;
-#pragma unroll 8
-      for (int s = 0; s < n_slices; ++s) t = __fadd_rn(t, p[s * step]);
+  float t = 0.0f;
+  if (row < M) {
+    const float* p = part + (int64_t)out * Mpad + row;
+    const int64_t step = (int64_t)kPartStride * Mpad;
+    int s = 0;
+    for (; s + kReduceBatch <= n_slices; s += kReduceBatch) {
+      float v[kReduceBatch];
+#pragma unroll
+      for (int q = 0; q < kReduceBatch; ++q) v[q] = __ldg(p + (int64_t)(s + q) * step);
+#pragma unroll
+      for (int q = 0; q < kReduceBatch; ++q) t = __fadd_rn(t, v[q]);
     }
-    s_tot[j][lane] = t;
+    for (; s < n_slices; ++s) t = __fadd_rn(t, __ldg(p + (int64_t)s * step));
   }
+  s_tot[out][lane] = t;
   __syncthreads();
-  if (warp != 0 || row >= M) return;
+  if (out != 0 || row >= M) return;
   float mixv[kMix];
 #pragma unroll
   for (int j = 0; j < kMix; ++j) mixv[j] = s_tot[j][lane];
