@@ -28,10 +28,10 @@ hcmix_reduce_kernel(const float* __restrict__ part, int n_slices, int Mpad, int 
                     float* __restrict__ mix_out, float* __restrict__ sq_out, int do_epilogue) {
   __shared__ float s_tot[kPartStride][kReduceRows + 1];
   const int lane = threadIdx.x & 31, out = threadIdx.x >> 5;  // out: mix index or 24 (sq)
-  const int row = blockIdx.x * kReduceRows + lane;
+  const int lrow = blockIdx.x * kReduceRows + lane;
   float t = 0.0f;
-  if (row < M) {
-    const float* p = part + (int64_t)out * Mpad + row;
+  if (lrow < M) {
+    const float* p = part + (int64_t)out * Mpad + lrow;
     const int64_t step = (int64_t)kPartStride * Mpad;
     int s = 0;
     for (; s + kReduceBatch <= n_slices; s += kReduceBatch) {
@@ -45,21 +45,50 @@ hcmix_reduce_kernel(const float* __restrict__ part, int n_slices, int Mpad, int 
   }
   s_tot[out][lane] = t;
   __syncthreads();
-  if (out != 0 || row >= M) return;
-  float mixv[kMix];
-#pragma unroll
-  for (int j = 0; j < kMix; ++j) mixv[j] = s_tot[j][lane];
-  const float sq = s_tot[kMix][lane];
-  if (mix_out != nullptr) {
-#pragma unroll
-    for (int j = 0; j < kMix; ++j) mix_out[(int64_t)row * kMix + j] = mixv[j];
+  const int tid = threadIdx.x;
+  const int row0 = blockIdx.x * kReduceRows;
+  if (mix_out != nullptr && tid < kReduceRows * kMix) {
+    const int r = tid / kMix, jj = tid % kMix;
+    if (row0 + r < M) mix_out[(int64_t)(row0 + r) * kMix + jj] = s_tot[jj][r];
   }
-  if (sq_out != nullptr) sq_out[row] = sq;
-  if (do_epilogue) {
-    epilogue_row(mixv, sq, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps,
-                 pre + (int64_t)row * kHc, post + (int64_t)row * kHc,
-                 comb + (int64_t)row * kHc * kHc);
+  if (sq_out != nullptr && tid < kReduceRows && row0 + tid < M) sq_out[row0 + tid] = s_tot[kMix][tid];
+  if (!do_epilogue || tid >= kReduceRows * kHc * kHc) return;
+
+  // Epilogue: 16 threads per row, thread e owns comb entry e = 4i + j and, for
+  // e < 8, logit e of pre (e < 4) or post.  Sinkhorn sums are gathered with
+  // shuffles and added in index order, as one thread per row would.
+  const int rloc = tid >> 4, e = tid & 15;
+  const int row = row0 + rloc;
+  const int gbase = threadIdx.x & 16;  // first lane of this row's 16-lane group
+  const float sq = s_tot[kMix][rloc];
+  const float v = __fadd_rn(__fmul_rn(sq, inv_k), rms_eps);
+  const float rr = __fdiv_rn(1.0f, __fsqrt_rn(v));
+  if (e < 2 * kHc) {
+    const float sc = e < kHc ? hc_scale[0] : hc_scale[1];
+    const float lg = __fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][rloc], rr), sc), hc_base[e]);
+    const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lg)));
+    if (row < M) {
+      if (e < kHc) pre[(int64_t)row * kHc + e] = sg;
+      else post[(int64_t)row * kHc + (e - kHc)] = __fmul_rn(2.0f, sg);
+    }
   }
+  const float lgc = __fadd_rn(__fmul_rn(__fmul_rn(s_tot[2 * kHc + e][rloc], rr), hc_scale[2]),
+                              hc_base[2 * kHc + e]);
+  float c = expf(lgc);
+  const int ci = e >> 2, cj = e & 3;
+  for (int it = 0; it < iters; ++it) {
+    float s = __shfl_sync(0xffffffffu, c, gbase + 4 * ci);
+    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 4 * ci + 1));
+    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 4 * ci + 2));
+    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 4 * ci + 3));
+    c = __fdiv_rn(c, __fadd_rn(s, hc_eps));
+    s = __shfl_sync(0xffffffffu, c, gbase + cj);
+    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 4 + cj));
+    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 8 + cj));
+    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 12 + cj));
+    c = __fdiv_rn(c, __fadd_rn(s, hc_eps));
+  }
+  if (row < M) comb[(int64_t)row * kHc * kHc + e] = c;
 }
 
 // The epilogue alone from caller-provided mix[M, 24] and sq[M].

@@ -8,8 +8,9 @@
 // slices in slice order.
 //
 // Per 64-column chunk (see hcmix_common.cuh for the numerics):
-//   * warp 0 (one thread) loads the x tile [128 rows x 64] and the four W limbs
-//     [96 rows x 64] with TMA (128-byte swizzle) into one of 6 stages;
+//   * warp 0 (one thread) loads the x tile [128 rows x 64] into a 9-stage ring
+//     and warp 2 (one thread) the four W limbs [96 rows x 64] into a 4-stage
+//     ring, both with TMA (128-byte swizzle);
 //   * a compute warpgroup (one thread per row) reads its row from shared
 //     memory, sums the squares with the page's tree, splits x into the limbs
 //     x0 (grid-aligned) and x1 = x - x0, and stores both into its TMEM A area;
@@ -19,8 +20,10 @@
 //       D = [x0.w0 | x0.w1 + x1.w0 | x0.w2 + x1.w1 | x0.w3 + x1.w2]
 //     (the first 24 columns are exact; x1.w3 ~ 2^-34 relative is dropped);
 //   * the warpgroup reads D and forms the chunk dot fl32(top + rest).
-// Three warpgroups work on three units at a time, so transforms, MMAs and
-// epilogues of different units overlap; TMEM holds 3 x (64 A + 96 D) columns.
+// Two warpgroups work on two units at a time.  Each is software-pipelined: it
+// transforms chunk k+1 into its second TMEM A buffer before it waits for the
+// MMAs of chunk k, so the MMA latency hides behind the next transform; D is
+// released together with A(k+1).  TMEM holds 2 x (2 x 64 A + 96 D) columns.
 #pragma once
 
 #include <cuda.h>
@@ -34,9 +37,11 @@
 namespace hcmix {
 namespace tc {
 
-constexpr int kStages = 6;
-constexpr int kWG = 3;
-constexpr int kWarps = 2 + 4 * kWG;
+constexpr int kXStages = 9;                                 // x tiles in flight
+constexpr int kBStages = 4;                                 // W limb tiles in flight
+constexpr int kWG = 2;
+constexpr int kFirstComputeWarp = 3;  // warp 0: x loads, 1: MMA, 2: W loads
+constexpr int kWarps = kFirstComputeWarp + 4 * kWG;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileM = 128;
 constexpr uint32_t kRowBytes = 128;                       // 64 bf16 per smem row
@@ -44,20 +49,22 @@ constexpr uint32_t kXBytes = kTileM * kRowBytes;          // x tile
 constexpr uint32_t kBBytes = 128 * kRowBytes;             // B buffer, 128 rows
 constexpr uint32_t kLimbRows = 4 * kMix;                  // w0..w3, 24 rows each
 constexpr uint32_t kLimbRowOffset = kMix;                 // limbs occupy B rows 24..119
-constexpr uint32_t kStageBytes = kXBytes + kBBytes;
-constexpr uint32_t kTxBytes = kXBytes + kLimbRows * kRowBytes;
+constexpr uint32_t kXTxBytes = kXBytes;
+constexpr uint32_t kBTxBytes = kLimbRows * kRowBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACols = 64;                           // x0: 32 columns, x1: 32 columns
 constexpr uint32_t kN = 96;
-constexpr uint32_t kWGCols = kACols + kN;
+constexpr uint32_t kWGCols = 2 * kACols + kN;             // two A buffers and one D per warpgroup
 constexpr uint32_t kIdesc = sm100::idesc_bf16_f32(128, kN);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;          // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 500000000ull;
 constexpr uint32_t kWarpArrivals = 4;                      // one arrive per warp of a warpgroup
 
 struct Bookkeeping {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full_x[kXStages];
+  uint64_t empty_x[kXStages];
+  uint64_t full_b[kBStages];
+  uint64_t empty_b[kBStages];
   uint64_t a_ready[kWG];
   uint64_t d_ready[kWG];
   uint64_t drain;
@@ -66,7 +73,8 @@ struct Bookkeeping {
   int never;  // stays 0: the abort flag of waits that must not be cut short
 };
 
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 1024;
+constexpr size_t kRingBytes = (size_t)kXStages * kXBytes + (size_t)kBStages * kBBytes;
+constexpr size_t kSmemBytes = kRingBytes + 1024 + 1024;
 
 static_assert(kWG * kWGCols <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Bookkeeping) <= 1024, "bookkeeping area");
@@ -132,9 +140,15 @@ constexpr uint32_t kBf16x2One = 0x3f803f80u;
 // largest |x| (exponent ex).  (x + magic) - magic rounds x to the grid
 // 2^(ex-5).  0 (no split) when the constant would not be a finite bf16.
 __device__ __forceinline__ uint32_t bf16x2_split_magic(const uint32_t (&w)[32]) {
-  uint32_t m = w[0];
+  uint32_t t[16];
 #pragma unroll
-  for (int i = 1; i < 32; ++i) m = sm100::bf16x2_max_abs(m, w[i]);
+  for (int i = 0; i < 16; ++i) t[i] = sm100::bf16x2_max_abs(w[i], w[i + 16]);
+#pragma unroll
+  for (int n = 8; n > 0; n >>= 1) {
+#pragma unroll
+    for (int i = 0; i < n; ++i) t[i] = sm100::bf16x2_max_abs(t[i], t[i + n]);
+  }
+  const uint32_t m = t[0];
   uint32_t f = max((m >> 7) & 0xffu, (m >> 23) & 0xffu);
   f = f < 1u ? 1u : f;
   if (f > 252u) return 0u;
@@ -188,21 +202,25 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Bookkeeping& bk = *reinterpret_cast<Bookkeeping*>(smem + (size_t)kStages * kStageBytes);
+  Bookkeeping& bk = *reinterpret_cast<Bookkeeping*>(smem + kRingBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int64_t G = gridDim.x, b = blockIdx.x;
   const int64_t u_begin = b * n_units / G;
   const int n = (int)((b + 1) * n_units / G - u_begin);
 
-  auto x_smem = [&](int st) { return smem + (size_t)st * kStageBytes; };
-  auto b_smem = [&](int st) { return smem + (size_t)st * kStageBytes + kXBytes; };
+  auto x_smem = [&](int st) { return smem + (size_t)st * kXBytes; };
+  auto b_smem = [&](int st) { return smem + (size_t)kXStages * kXBytes + (size_t)st * kBBytes; };
 
   // ---- set-up: barriers, the zero rows of every B buffer, TMEM
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bk.full[s]), 1);
-      mbar_init(smem_u32(&bk.empty[s]), kWarpArrivals + 1);
+    for (int s = 0; s < kXStages; ++s) {
+      mbar_init(smem_u32(&bk.full_x[s]), 1);
+      mbar_init(smem_u32(&bk.empty_x[s]), kWarpArrivals);
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(smem_u32(&bk.full_b[s]), 1);
+      mbar_init(smem_u32(&bk.empty_b[s]), 1);
     }
     for (int g = 0; g < kWG; ++g) {
       mbar_init(smem_u32(&bk.a_ready[g]), kWarpArrivals);
@@ -216,7 +234,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   {
     // rows 0..23 (3072 B) and 120..127 (1024 B) of each B buffer stay zero
     constexpr int kUnits = (3072 + 1024) / 16;
-    for (int idx = threadIdx.x; idx < kStages * kUnits; idx += kThreads) {
+    for (int idx = threadIdx.x; idx < kBStages * kUnits; idx += kThreads) {
       const int s = idx / kUnits, u = idx % kUnits;
       const uint32_t off = u < 192 ? (uint32_t)u * 16 : 120 * kRowBytes + (uint32_t)(u - 192) * 16;
       *reinterpret_cast<uint4*>(b_smem(s) + off) = make_uint4(0, 0, 0, 0);
@@ -234,13 +252,18 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const volatile int* abort_flag = &bk.abort;
   const volatile int* never = &bk.never;
 
-  if (warp == 0) {
-    // ---------------- TMA producer
+  if (warp == 0 || warp == 2) {
+    // ---------------- TMA producers: warp 0 streams x tiles (released as soon
+    // as a warpgroup has read them), warp 2 the W limb tiles (released by the
+    // MMA commit); separate rings keep many x tiles in flight
     if (lane == 0) {
-      prefetch_tensormap(&tmap_x);
-      prefetch_tensormap(&tmap_w);
-      const uint64_t pol_x = l2_policy_evict_first();
-      const uint64_t pol_w = l2_policy_evict_last();
+      const bool is_x = warp == 0;
+      const int nst = is_x ? kXStages : kBStages;
+      uint64_t* fullb = is_x ? bk.full_x : bk.full_b;
+      uint64_t* emptyb = is_x ? bk.empty_x : bk.empty_b;
+      const void* map = is_x ? static_cast<const void*>(&tmap_x) : static_cast<const void*>(&tmap_w);
+      prefetch_tensormap(map);
+      const uint64_t pol = is_x ? l2_policy_evict_first() : l2_policy_evict_last();
       int i = 0;
       bool ok = true;
       for (int r = 0; ok && kWG * r < n; ++r) {
@@ -250,170 +273,198 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
             const int64_t unit = u_begin + kWG * r + g;
             const int tile = (int)(unit / n_slices), s = (int)(unit % n_slices);
             const int k0 = s * kSlice + c * kChunk;
-            const int st = i % kStages;
-            const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-            if (i >= kStages &&
-                !mbar_wait(smem_u32(&bk.empty[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+            const int st = i % nst;
+            const uint32_t ph = (uint32_t)(i / nst) & 1u;
+            if (i >= nst &&
+                !mbar_wait(smem_u32(&emptyb[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
               fail(bk, err);
               ok = false;
               break;
             }
-            const uint32_t full = smem_u32(&bk.full[st]);
-            mbar_arrive_expect_tx(full, kTxBytes);
-            tma_load_2d(smem_u32(x_smem(st)), &tmap_x, k0, tile * kTileM, full, pol_x);
-            tma_load_2d(smem_u32(b_smem(st)) + kLimbRowOffset * kRowBytes, &tmap_w, k0, 0, full,
-                        pol_w);
+            const uint32_t full = smem_u32(&fullb[st]);
+            if (is_x) {
+              mbar_arrive_expect_tx(full, kXTxBytes);
+              tma_load_2d(smem_u32(x_smem(st)), map, k0, tile * kTileM, full, pol);
+            } else {
+              mbar_arrive_expect_tx(full, kBTxBytes);
+              tma_load_2d(smem_u32(b_smem(st)) + kLimbRowOffset * kRowBytes, map, k0, 0, full, pol);
+            }
           }
         }
       }
       // drain: the loads still in flight complete before the CTA can exit
-      for (int j = max(0, i - kStages); j < i; ++j)
-        mbar_wait(smem_u32(&bk.full[j % kStages]), (uint32_t)(j / kStages) & 1u, never,
-                  kDrainLimitNs);
+      for (int j = max(0, i - nst); j < i; ++j)
+        mbar_wait(smem_u32(&fullb[j % nst]), (uint32_t)(j / nst) & 1u, never, kDrainLimitNs);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: chunks in sequence order.  Chunk i needs its
+    // warpgroup's x limbs (a_ready) and its W limb tile (full_b); both waits
+    // suspend the thread.  In order, the W tile of chunk i only depends on the
+    // MMAs of earlier chunks, so no wait can close a cycle.
     if (lane == 0) {
-      int cnt[kWG] = {0, 0, 0};
+      int done[kWG] = {0, 0};
       int i = 0;
       bool ok = true;
       for (int r = 0; ok && kWG * r < n; ++r) {
         const int act = min(kWG, n - kWG * r);
         for (int c = 0; ok && c < kChunksPerSlice; ++c) {
           for (int g = 0; g < act; ++g, ++i) {
-            const int st = i % kStages;
-            const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-            if (!mbar_wait(smem_u32(&bk.a_ready[g]), (uint32_t)cnt[g] & 1u, abort_flag,
+            const int st = i % kBStages;
+            const uint32_t ph = (uint32_t)(i / kBStages) & 1u;
+            if (!mbar_wait(smem_u32(&bk.a_ready[g]), (uint32_t)done[g] & 1u, abort_flag,
                            kWaitLimitNs) ||
-                !mbar_wait(smem_u32(&bk.full[st]), ph, abort_flag, kWaitLimitNs)) {
-              fail(bk, err);
+                !mbar_wait(smem_u32(&bk.full_b[st]), ph, abort_flag, kWaitLimitNs)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a = tmem + (uint32_t)g * kWGCols;
-            const uint32_t d = a + kACols;
+            const uint32_t a = tmem + (uint32_t)g * kWGCols + (uint32_t)(done[g] & 1) * kACols;
+            const uint32_t d = tmem + (uint32_t)g * kWGCols + 2 * kACols;
             const uint32_t bb = smem_u32(b_smem(st));
 #pragma unroll
             for (int q = 0; q < 4; ++q)  // x1 against [0 | w0 | w1 | w2]
               umma_bf16_ts(d, a + 32 + 8 * q, smem_desc_sw128(bb + 32 * q), kIdesc, q > 0);
 #pragma unroll
             for (int q = 0; q < 4; ++q)  // x0 against [w0 | w1 | w2 | w3]
-              umma_bf16_ts(d, a + 8 * q,
-                           smem_desc_sw128(bb + kLimbRowOffset * kRowBytes + 32 * q), kIdesc, 1);
+              umma_bf16_ts(d, a + 8 * q, smem_desc_sw128(bb + kLimbRowOffset * kRowBytes + 32 * q),
+                           kIdesc, 1);
             umma_commit(smem_u32(&bk.d_ready[g]));
-            umma_commit(smem_u32(&bk.empty[st]));
-            ++cnt[g];
+            umma_commit(smem_u32(&bk.empty_b[st]));
+            ++done[g];
           }
         }
       }
+      if (!ok) fail(bk, err);
       umma_commit(smem_u32(&bk.drain));
       mbar_wait(smem_u32(&bk.drain), 0, never, kDrainLimitNs);
     }
   } else {
     // ---------------- compute warpgroups: one thread per tile row
-    const int g = (warp - 2) >> 2;
+    const int g = (warp - kFirstComputeWarp) >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t a_col = tmem + (uint32_t)g * kWGCols;
-    const uint32_t d_col = a_col + kACols;
-    int cnt = 0;
-    bool ok = true;
-    for (int r = 0; ok && kWG * r + g < n; ++r) {
+    const uint32_t a_base = tmem + (uint32_t)g * kWGCols;
+    const uint32_t d_col = a_base + 2 * kACols;
+    // byte offsets of the row's 16-byte pieces p in a swizzled x tile
+    uint32_t xoff[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) xoff[p] = (uint32_t)row * kRowBytes + ((uint32_t)(p ^ (row & 7)) << 4);
+    const int my_units = (n - g + kWG - 1) / kWG;
+    const int my_chunks = kChunksPerSlice * my_units;
+
+    // transform of this warpgroup's chunk k: sum of squares and the x limbs
+    // into A buffer k % 2; returns the chunk's sum of squares
+    auto transform = [&](int k, float& tsq) -> bool {
+      const int r = k / kChunksPerSlice, c = k % kChunksPerSlice;
       const int act = min(kWG, n - kWG * r);
-      const int64_t unit = u_begin + kWG * r + g;
-      const int tile = (int)(unit / n_slices), s = (int)(unit % n_slices);
-      float2 acc[kMix / 2];
+      const int i = seq_index(r, c, g, act);
+      const int st = i % kXStages;
+      const uint32_t ph = (uint32_t)(i / kXStages) & 1u;
+      bool ok = mbar_wait(smem_u32(&bk.full_x[st]), ph, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) return false;
+      const uint8_t* xt = x_smem(st);
+      uint32_t xw[32];
 #pragma unroll
-      for (int j = 0; j < kMix / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-      float sqs = 0.0f;
-      for (int c = 0; c < kChunksPerSlice; ++c) {
-        const int i = seq_index(r, c, g, act);
-        const int st = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        ok = mbar_wait(smem_u32(&bk.full[st]), ph, abort_flag, kWaitLimitNs);
-        ok = __all_sync(0xffffffffu, ok);
+      for (int p = 0; p < 8; ++p) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xt + xoff[p]);
+        xw[4 * p] = v.x; xw[4 * p + 1] = v.y; xw[4 * p + 2] = v.z; xw[4 * p + 3] = v.w;
+      }
+      tsq = sq_tree64_f32x2(xw);
+      // x0 = x rounded to the grid 2^(ex-5) with the bf16 magic constant
+      // 1.5 * 2^(ex+2) (x + magic stays in one binade, so one bf16 rounding
+      // puts x on the grid); x1 = x - x0 is exact.  Both are bf16, <= 8 bits.
+      const uint32_t magic = bf16x2_split_magic(xw);
+      const uint32_t a_col = a_base + (uint32_t)(k & 1) * kACols;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w0[16], w1[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const uint32_t wd = xw[16 * half + t];
+          w0[t] = bf16x2_sub(bf16x2_fma(wd, kBf16x2One, magic), magic);
+          w1[t] = bf16x2_sub(wd, w0[t]);
+        }
+        tmem_st16(lanes | (a_col + 16 * half), w0);
+        tmem_st16(lanes | (a_col + 32 + 16 * half), w1);
+      }
+      tmem_wait_st();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bk.empty_x[st]));  // x tile read
+      return true;
+    };
+
+    float2 acc[kMix / 2];
+#pragma unroll
+    for (int j = 0; j < kMix / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+    float sqs = 0.0f, tsq_cur = 0.0f, tsq_next = 0.0f;
+    bool ok = my_chunks > 0 ? transform(0, tsq_cur) : true;
+    if (ok && my_chunks > 0) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bk.a_ready[g]));
+    }
+    for (int k = 0; ok && k < my_chunks; ++k) {
+      if (k + 1 < my_chunks) {
+        ok = transform(k + 1, tsq_next);
         if (!ok) break;
-        // the row's 64 values: 16-byte piece p sits at p ^ (row & 7) (128-byte swizzle)
-        const uint8_t* xrow = x_smem(st) + row * kRowBytes;
-        uint32_t xw[32];
+      }
+      ok = mbar_wait(smem_u32(&bk.d_ready[g]), (uint32_t)k & 1u, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      // D = [top | r1 | r2 | r3]; chunk dot = top + ((r1 + r2) + r3), in output pairs
+      {
+        uint32_t rr[3][kMix];
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xrow + ((p ^ (row & 7)) << 4));
-          xw[4 * p] = v.x; xw[4 * p + 1] = v.y; xw[4 * p + 2] = v.z; xw[4 * p + 3] = v.w;
+        for (int q = 0; q < 3; ++q) {
+          tmem_ld16(lanes | (d_col + 24 * (q + 1)), rr[q]);
+          tmem_ld8(lanes | (d_col + 24 * (q + 1) + 16), rr[q] + 16);
         }
-        sqs = __fadd_rn(sqs, sq_tree64_f32x2(xw));
-        // x0 = x rounded to the grid 2^(ex-5) with the bf16 magic constant
-        // 1.5 * 2^(ex+2) (x + magic stays in one binade, so one bf16 rounding puts
-        // x on the grid); x1 = x - x0 is exact.  Both are bf16 with <= 8 bits.
-        const uint32_t magic = bf16x2_split_magic(xw);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t w0[16], w1[16];
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const uint32_t wd = xw[16 * half + t];
-            w0[t] = bf16x2_sub(bf16x2_fma(wd, kBf16x2One, magic), magic);
-            w1[t] = bf16x2_sub(wd, w0[t]);
-          }
-          tmem_st16(lanes | (a_col + 16 * half), w0);
-          tmem_st16(lanes | (a_col + 32 + 16 * half), w1);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&bk.a_ready[g]));
-          mbar_arrive(smem_u32(&bk.empty[st]));
-        }
-        ok = mbar_wait(smem_u32(&bk.d_ready[g]), (uint32_t)cnt & 1u, abort_flag, kWaitLimitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        ++cnt;
-        tc_fence_after();
-        // D = [top | r1 | r2 | r3]; chunk dot = top + ((r1 + r2) + r3), in output pairs
-        uint32_t top[kMix], t[kMix];
+        tmem_wait_ld();
         float2 rest[kMix / 2];
+#pragma unroll
+        for (int j = 0; j < kMix / 2; ++j) {
+          const float2 u = make_float2(__uint_as_float(rr[0][2 * j]), __uint_as_float(rr[0][2 * j + 1]));
+          const float2 v = make_float2(__uint_as_float(rr[1][2 * j]), __uint_as_float(rr[1][2 * j + 1]));
+          const float2 w = make_float2(__uint_as_float(rr[2][2 * j]), __uint_as_float(rr[2][2 * j + 1]));
+          rest[j] = __fadd2_rn(__fadd2_rn(u, v), w);
+        }
+        uint32_t top[kMix];
         tmem_ld16(lanes | d_col, top);
         tmem_ld8(lanes | (d_col + 16), top + 16);
-        tmem_ld16(lanes | (d_col + 24), t);
-        tmem_ld8(lanes | (d_col + 40), t + 16);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < kMix / 2; ++j)
-          rest[j] = make_float2(__uint_as_float(t[2 * j]), __uint_as_float(t[2 * j + 1]));
-        tmem_ld16(lanes | (d_col + 48), t);
-        tmem_ld8(lanes | (d_col + 64), t + 16);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < kMix / 2; ++j)
-          rest[j] = __fadd2_rn(
-              rest[j], make_float2(__uint_as_float(t[2 * j]), __uint_as_float(t[2 * j + 1])));
-        tmem_ld16(lanes | (d_col + 72), t);
-        tmem_ld8(lanes | (d_col + 88), t + 16);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < kMix / 2; ++j) {
-          rest[j] = __fadd2_rn(
-              rest[j], make_float2(__uint_as_float(t[2 * j]), __uint_as_float(t[2 * j + 1])));
           const float2 d = __fadd2_rn(
               make_float2(__uint_as_float(top[2 * j]), __uint_as_float(top[2 * j + 1])), rest[j]);
           acc[j] = __fadd2_rn(acc[j], d);
         }
       }
-      if (!ok) {
-        fail(bk, err);
-        break;
+      sqs = __fadd_rn(sqs, tsq_cur);
+      tsq_cur = tsq_next;
+      // A(k+1) is written and D has been read: the MMAs of chunk k+1 may run
+      if (k + 1 < my_chunks) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bk.a_ready[g]));
       }
-      float* p = part + (int64_t)s * kPartStride * Mpad + (int64_t)tile * kTileM + row;
+      if (k % kChunksPerSlice == kChunksPerSlice - 1) {
+        const int64_t unit = u_begin + kWG * (k / kChunksPerSlice) + g;
+        const int tile = (int)(unit / n_slices), s = (int)(unit % n_slices);
+        float* p = part + (int64_t)s * kPartStride * Mpad + (int64_t)tile * kTileM + row;
 #pragma unroll
-      for (int j = 0; j < kMix / 2; ++j) {
-        p[(int64_t)(2 * j) * Mpad] = acc[j].x;
-        p[(int64_t)(2 * j + 1) * Mpad] = acc[j].y;
+        for (int j = 0; j < kMix / 2; ++j) {
+          p[(int64_t)(2 * j) * Mpad] = acc[j].x;
+          p[(int64_t)(2 * j + 1) * Mpad] = acc[j].y;
+          acc[j] = make_float2(0.0f, 0.0f);
+        }
+        p[(int64_t)kMix * Mpad] = sqs;
+        sqs = 0.0f;
       }
-      p[(int64_t)kMix * Mpad] = sqs;
     }
+    if (!ok) fail(bk, err);
   }
 
   // ---- teardown: every role has finished (or given up); free TMEM
