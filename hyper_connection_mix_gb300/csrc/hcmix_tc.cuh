@@ -1,24 +1,28 @@
 // Tensor-core (tcgen05) contraction path for sm_103a.
 //
 // Work: the rows are cut into 128-row tiles and K into 256-column slices (the
-// hc_fused page's slice grid); a unit is one (tile, slice) pair.  Each CTA of
-// a grid of min(#SMs, #units) takes a contiguous range of units and writes,
-// for each unit, the slice totals of its 128 rows (24 mix values and the sum
-// of squares) to the workspace partials; hcmix_reduce_kernel then adds the
+// hc_fused page's slice grid); a unit is one (tile, slice) pair, numbered
+// slice-major.  Each CTA of a grid of min(#SMs, #units) takes a contiguous
+// range of units, so its units mostly share one slice, and writes, for each
+// unit, the slice totals of its 128 rows (24 mix values and the sum of
+// squares) to the workspace partials; hcmix_reduce_kernel then adds the
 // slices in slice order.
 //
 // Per 64-column chunk (see hcmix_common.cuh for the numerics):
-//   * warp 0 (one thread) loads the x tile [128 rows x 64] into a 9-stage ring
-//     and warp 2 (one thread) the four W limbs [96 rows x 64] into a 4-stage
-//     ring, both with TMA (128-byte swizzle);
+//   * warp 0 (one thread) loads x with TMA, two chunks of a tile (32 KB) per
+//     load, into a 3-stage ring; warp 2 (one thread) loads the four W limbs of
+//     a slice [96 rows x 64 per chunk] into the B buffers of a warpgroup when
+//     that warpgroup reaches a new slice (128-byte swizzle for both);
 //   * a compute warpgroup (one thread per row) reads its row from shared
 //     memory, sums the squares with the page's tree, splits x into the limbs
 //     x0 (grid-aligned) and x1 = x - x0, and stores both into its TMEM A area;
-//   * warp 1 (one thread) issues 8 MMAs of M=128, N=96, K=16 with A in TMEM
-//     and B in shared memory:  B rows [0 | w0 | w1 | w2] against x1, then
-//     [w0 | w1 | w2 | w3] against x0, accumulating into the warpgroup's TMEM D:
+//   * warp 1 issues 8 MMAs of M=128, N=96, K=16 with A in TMEM and B in shared
+//     memory:  B rows [0 | w0 | w1 | w2] against x1, then [w0 | w1 | w2 | w3]
+//     against x0, accumulating into the warpgroup's TMEM D:
 //       D = [x0.w0 | x0.w1 + x1.w0 | x0.w2 + x1.w1 | x0.w3 + x1.w2]
 //     (the first 24 columns are exact; x1.w3 ~ 2^-34 relative is dropped);
+//     the whole warp runs the issue loop and one elected lane issues, which
+//     keeps the loop warp-uniform (twice the MMA rate of a one-lane loop);
 //   * the warpgroup reads D and forms the chunk dot fl32(top + rest).
 // Two warpgroups work on two units at a time.  Each is software-pipelined: it
 // transforms chunk k+1 into its second TMEM A buffer before it waits for the
@@ -37,16 +41,22 @@
 namespace hcmix {
 namespace tc {
 
-constexpr int kXStages = 9;                                 // x tiles in flight
-constexpr int kBStages = 4;                                 // W limb tiles in flight
+constexpr int kXStages = 3;                                 // x stages in flight
+constexpr int kChunksPerStage = 2;  // an x stage holds two chunks of a tile (one 32 KB load)
 constexpr int kWG = 2;
+// Units run slice-major, so a CTA's units mostly share one slice and the W
+// limbs of a slice (one B buffer per chunk) stay in shared memory across
+// them; each warpgroup has its own set, reloaded when its slice changes.
+constexpr int kBStages = kWG * kChunksPerSlice;
 constexpr int kFirstComputeWarp = 3;  // warp 0: x loads, 1: MMA, 2: W loads
 constexpr int kWarps = kFirstComputeWarp + 4 * kWG;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileM = 128;
 constexpr uint32_t kRowBytes = 128;                       // 64 bf16 per smem row
-constexpr uint32_t kXBytes = kTileM * kRowBytes;          // x tile
-constexpr uint32_t kBBytes = 128 * kRowBytes;             // B buffer, 128 rows
+constexpr uint32_t kXChunkBytes = kTileM * kRowBytes;     // one chunk of a tile
+constexpr uint32_t kXBytes = kChunksPerStage * kXChunkBytes;  // x stage
+constexpr uint32_t kBRows = 120;                          // B rows the MMAs read
+constexpr uint32_t kBBytes = kBRows * kRowBytes;          // B buffer
 constexpr uint32_t kLimbRows = 4 * kMix;                  // w0..w3, 24 rows each
 constexpr uint32_t kLimbRowOffset = kMix;                 // limbs occupy B rows 24..119
 constexpr uint32_t kXTxBytes = kXBytes;
@@ -78,6 +88,9 @@ constexpr size_t kSmemBytes = kRingBytes + 1024 + 1024;
 
 static_assert(kWG * kWGCols <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Bookkeeping) <= 1024, "bookkeeping area");
+static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of one slice");
+static_assert(kSmemBytes <= 232448, "dynamic shared memory");
+static_assert(kBBytes % 1024 == 0 && kLimbRowOffset + kLimbRows <= kBRows, "B buffer layout");
 
 // ---------------------------------------------------------------- W limbs
 
@@ -157,28 +170,27 @@ __device__ __forceinline__ uint32_t bf16x2_split_magic(const uint32_t (&w)[32]) 
 }
 
 // The page's sum-of-squares tree (column bits 4, 3, 2, 1, 0, then the two
-// halves) on 32 packed words, with the pair sums of bits 4..1 done two at a
-// time: word w holds columns 2w (low half) and 2w+1 (high half), so columns
-// differing in bit b >= 1 sit in words differing in bit b-1 at the same half.
+// halves) on 32 packed words: word w holds columns 2w (low half) and 2w+1
+// (high half), so columns differing in bit b >= 1 sit in words differing in
+// bit b-1 at the same half.  The bit-4 level fl(x_c^2 + x_{c+16}^2) is one
+// mixed-precision FMA on an exact square; the pair sums of bits 3..1 are done
+// two at a time.
 __device__ __forceinline__ float sq_tree64_f32x2(const uint32_t (&w)[32]) {
-  float2 v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float2 u = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
-    v[i] = __fmul2_rn(u, u);
-  }
   float h[2];
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    float2* q = v + 16 * half;
+    const uint32_t* q = w + 16 * half;
+    float2 v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fadd2_rn(q[i], q[i + 8]);  // column bit 4
+    for (int i = 0; i < 8; ++i)  // column bit 4: words i and i + 8
+      v[i] = make_float2(sm100::fma_sq_bf16_lo(q[i], sm100::fma_sq_bf16_lo(q[i + 8], 0.0f)),
+                         sm100::fma_sq_bf16_hi(q[i], sm100::fma_sq_bf16_hi(q[i + 8], 0.0f)));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = __fadd2_rn(q[i], q[i + 4]);  // bit 3
+    for (int i = 0; i < 4; ++i) v[i] = __fadd2_rn(v[i], v[i + 4]);  // bit 3
 #pragma unroll
-    for (int i = 0; i < 2; ++i) q[i] = __fadd2_rn(q[i], q[i + 2]);  // bit 2
-    q[0] = __fadd2_rn(q[0], q[1]);                                   // bit 1
-    h[half] = __fadd_rn(q[0].x, q[0].y);                             // bit 0
+    for (int i = 0; i < 2; ++i) v[i] = __fadd2_rn(v[i], v[i + 2]);  // bit 2
+    v[0] = __fadd2_rn(v[0], v[1]);                                   // bit 1
+    h[half] = __fadd_rn(v[0].x, v[0].y);                             // bit 0
   }
   return __fadd_rn(h[0], h[1]);                                      // the two halves
 }
@@ -188,15 +200,9 @@ __device__ __forceinline__ void fail(Bookkeeping& bk, uint32_t* err) {
   *reinterpret_cast<volatile int*>(&bk.abort) = 1;
 }
 
-// Sequence index of chunk c of round r for warpgroup g (rounds before the last
-// are full, so they hold kWG * kChunksPerSlice chunks each).
-__device__ __forceinline__ int seq_index(int r, int c, int g, int act) {
-  return r * kWG * kChunksPerSlice + c * act + g;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                const __grid_constant__ CUtensorMap tmap_w, int n_slices, int Mpad,
+                const __grid_constant__ CUtensorMap tmap_w, int n_tiles, int Mpad,
                 int64_t n_units, float* __restrict__ part, uint32_t* __restrict__ err) {
   using namespace sm100;
   extern __shared__ uint8_t smem_raw[];
@@ -232,12 +238,11 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     fence_mbarrier_init();
   }
   {
-    // rows 0..23 (3072 B) and 120..127 (1024 B) of each B buffer stay zero
-    constexpr int kUnits = (3072 + 1024) / 16;
+    // rows 0..23 of each B buffer stay zero (the limbs are loaded to rows 24..119)
+    constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
     for (int idx = threadIdx.x; idx < kBStages * kUnits; idx += kThreads) {
       const int s = idx / kUnits, u = idx % kUnits;
-      const uint32_t off = u < 192 ? (uint32_t)u * 16 : 120 * kRowBytes + (uint32_t)(u - 192) * 16;
-      *reinterpret_cast<uint4*>(b_smem(s) + off) = make_uint4(0, 0, 0, 0);
+      sts128(smem_u32(b_smem(s)) + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
     }
     fence_proxy_async_smem();
   }
@@ -252,92 +257,159 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const volatile int* abort_flag = &bk.abort;
   const volatile int* never = &bk.never;
 
-  if (warp == 0 || warp == 2) {
-    // ---------------- TMA producers: warp 0 streams x tiles (released as soon
-    // as a warpgroup has read them), warp 2 the W limb tiles (released by the
-    // MMA commit); separate rings keep many x tiles in flight
+  // units are slice-major: unit u is tile u % n_tiles of slice u / n_tiles
+  auto unit_tile = [&](int64_t u) { return (int)(u % n_tiles); };
+  auto unit_slice = [&](int64_t u) { return (int)(u / n_tiles); };
+
+  if (warp == 0) {
+    // ---------------- x producer: stage i holds two chunks of one unit, in
+    // the order (round, chunk pair, warpgroup); released by the warpgroup
     if (lane == 0) {
-      const bool is_x = warp == 0;
-      const int nst = is_x ? kXStages : kBStages;
-      uint64_t* fullb = is_x ? bk.full_x : bk.full_b;
-      uint64_t* emptyb = is_x ? bk.empty_x : bk.empty_b;
-      const void* map = is_x ? static_cast<const void*>(&tmap_x) : static_cast<const void*>(&tmap_w);
-      prefetch_tensormap(map);
-      const uint64_t pol = is_x ? l2_policy_evict_first() : l2_policy_evict_last();
+      prefetch_tensormap(&tmap_x);
+      const uint64_t pol = l2_policy_evict_first();
       int i = 0;
       bool ok = true;
       for (int r = 0; ok && kWG * r < n; ++r) {
         const int act = min(kWG, n - kWG * r);
-        for (int c = 0; ok && c < kChunksPerSlice; ++c) {
+        for (int c = 0; ok && c < kChunksPerSlice; c += kChunksPerStage) {
           for (int g = 0; g < act; ++g, ++i) {
             const int64_t unit = u_begin + kWG * r + g;
-            const int tile = (int)(unit / n_slices), s = (int)(unit % n_slices);
-            const int k0 = s * kSlice + c * kChunk;
-            const int st = i % nst;
-            const uint32_t ph = (uint32_t)(i / nst) & 1u;
-            if (i >= nst &&
-                !mbar_wait(smem_u32(&emptyb[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+            const int st = i % kXStages;
+            const uint32_t ph = (uint32_t)(i / kXStages) & 1u;
+            if (i >= kXStages &&
+                !mbar_wait(smem_u32(&bk.empty_x[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
               fail(bk, err);
               ok = false;
               break;
             }
-            const uint32_t full = smem_u32(&fullb[st]);
-            if (is_x) {
-              mbar_arrive_expect_tx(full, kXTxBytes);
-              tma_load_2d(smem_u32(x_smem(st)), map, k0, tile * kTileM, full, pol);
-            } else {
-              mbar_arrive_expect_tx(full, kBTxBytes);
-              tma_load_2d(smem_u32(b_smem(st)) + kLimbRowOffset * kRowBytes, map, k0, 0, full, pol);
-            }
+            const uint32_t full = smem_u32(&bk.full_x[st]);
+            mbar_arrive_expect_tx(full, kXTxBytes);
+            tma_load_3d(smem_u32(x_smem(st)), &tmap_x, 0, unit_tile(unit) * kTileM,
+                        unit_slice(unit) * kChunksPerSlice + c, full, pol);
           }
         }
       }
       // drain: the loads still in flight complete before the CTA can exit
-      for (int j = max(0, i - nst); j < i; ++j)
-        mbar_wait(smem_u32(&fullb[j % nst]), (uint32_t)(j / nst) & 1u, never, kDrainLimitNs);
+      for (int j = max(0, i - kXStages); j < i; ++j)
+        mbar_wait(smem_u32(&bk.full_x[j % kXStages]), (uint32_t)(j / kXStages) & 1u, never,
+                  kDrainLimitNs);
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer: chunks in sequence order.  Chunk i needs its
-    // warpgroup's x limbs (a_ready) and its W limb tile (full_b); both waits
-    // suspend the thread.  In order, the W tile of chunk i only depends on the
-    // MMAs of earlier chunks, so no wait can close a cycle.
+  } else if (warp == 2) {
+    // ---------------- W producer: when warpgroup g reaches a new slice, its
+    // four B buffers are reloaded with that slice's limbs, once the MMAs of
+    // its previous slice have released them (empty_b, committed after their
+    // last use)
     if (lane == 0) {
-      int done[kWG] = {0, 0};
-      int i = 0;
+      prefetch_tensormap(&tmap_w);
+      const uint64_t pol = l2_policy_evict_last();
+      int loads[kWG] = {0, 0}, cur[kWG] = {-1, -1};
       bool ok = true;
       for (int r = 0; ok && kWG * r < n; ++r) {
         const int act = min(kWG, n - kWG * r);
-        for (int c = 0; ok && c < kChunksPerSlice; ++c) {
-          for (int g = 0; g < act; ++g, ++i) {
-            const int st = i % kBStages;
-            const uint32_t ph = (uint32_t)(i / kBStages) & 1u;
-            if (!mbar_wait(smem_u32(&bk.a_ready[g]), (uint32_t)done[g] & 1u, abort_flag,
-                           kWaitLimitNs) ||
-                !mbar_wait(smem_u32(&bk.full_b[st]), ph, abort_flag, kWaitLimitNs)) {
+#pragma unroll
+        for (int g = 0; g < kWG; ++g) {
+          if (!ok || g >= act) continue;
+          const int sl = unit_slice(u_begin + kWG * r + g);
+          if (sl == cur[g]) continue;
+          cur[g] = sl;
+          for (int c = 0; c < kChunksPerSlice; ++c) {
+            const int j = g * kChunksPerSlice + c;
+            if (loads[g] > 0 && !mbar_wait(smem_u32(&bk.empty_b[j]),
+                                           (uint32_t)(loads[g] - 1) & 1u, abort_flag,
+                                           kWaitLimitNs)) {
+              fail(bk, err);
               ok = false;
               break;
             }
-            tc_fence_after();
-            const uint32_t a = tmem + (uint32_t)g * kWGCols + (uint32_t)(done[g] & 1) * kACols;
-            const uint32_t d = tmem + (uint32_t)g * kWGCols + 2 * kACols;
-            const uint32_t bb = smem_u32(b_smem(st));
-#pragma unroll
-            for (int q = 0; q < 4; ++q)  // x1 against [0 | w0 | w1 | w2]
-              umma_bf16_ts(d, a + 32 + 8 * q, smem_desc_sw128(bb + 32 * q), kIdesc, q > 0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)  // x0 against [w0 | w1 | w2 | w3]
-              umma_bf16_ts(d, a + 8 * q, smem_desc_sw128(bb + kLimbRowOffset * kRowBytes + 32 * q),
-                           kIdesc, 1);
-            umma_commit(smem_u32(&bk.d_ready[g]));
-            umma_commit(smem_u32(&bk.empty_b[st]));
-            ++done[g];
+            const uint32_t full = smem_u32(&bk.full_b[j]);
+            mbar_arrive_expect_tx(full, kBTxBytes);
+            tma_load_2d(smem_u32(b_smem(j)) + kLimbRowOffset * kRowBytes, &tmap_w,
+                        (sl * kChunksPerSlice + c) * kChunk, 0, full, pol);
           }
+          ++loads[g];
         }
       }
-      if (!ok) fail(bk, err);
-      umma_commit(smem_u32(&bk.drain));
-      mbar_wait(smem_u32(&bk.drain), 0, never, kDrainLimitNs);
+      // drain
+#pragma unroll
+      for (int g = 0; g < kWG; ++g)
+        if (loads[g] > 0)
+          for (int c = 0; c < kChunksPerSlice; ++c)
+            mbar_wait(smem_u32(&bk.full_b[g * kChunksPerSlice + c]), (uint32_t)(loads[g] - 1) & 1u,
+                      never, kDrainLimitNs);
     }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer, chunks in sequence order (round, chunk,
+    // warpgroup).  Chunk i needs its warpgroup's x limbs (a_ready) and the W
+    // limb tile of its slice (full_b, phase = the warpgroup's slice count).
+    // In order, each wait depends only on earlier chunks, so no wait can close
+    // a cycle.  The whole warp runs the loop, the waits are warp votes and one
+    // elected lane issues each MMA and commit: a loop whose control flow the
+    // compiler cannot prove warp-uniform issued MMAs at about half the rate.
+    // per warpgroup: slice of its current unit, B loads so far, and whether
+    // this round's unit is the last of its slice (tracked incrementally: the
+    // units of a round are consecutive)
+    int64_t u_tile = u_begin % n_tiles, u_slice = u_begin / n_tiles;  // of unit u_begin + kWG * r
+    int loads[kWG] = {0, 0}, cur[kWG] = {-1, -1};
+    bool ok = true;
+    for (int r = 0; ok && kWG * r < n; ++r) {
+      const int act = min(kWG, n - kWG * r);
+      int sl[kWG];
+      bool fresh[kWG], last_use[kWG];
+      {
+        int64_t t = u_tile, sv = u_slice;
+#pragma unroll
+        for (int g = 0; g < kWG; ++g) {
+          sl[g] = (int)sv;
+          fresh[g] = g < act && sl[g] != cur[g];
+          if (fresh[g]) {
+            cur[g] = sl[g];
+            ++loads[g];
+          }
+          if (++t == n_tiles) { t = 0; ++sv; }
+        }
+        u_tile = t;
+        u_slice = sv;
+        // unit + kWG of warpgroup g is unit kWG * (r + 1) + g: its slice
+#pragma unroll
+        for (int g = 0; g < kWG; ++g) {
+          int64_t t2 = t, s2 = sv;
+          for (int q = 0; q < g; ++q)
+            if (++t2 == n_tiles) { t2 = 0; ++s2; }
+          last_use[g] = kWG * (r + 1) + g >= n || (int)s2 != sl[g];
+        }
+      }
+      for (int c = 0; ok && c < kChunksPerSlice; ++c) {
+#pragma unroll
+        for (int g = 0; g < kWG; ++g) {
+          if (!ok || g >= act) continue;
+          const int j = g * kChunksPerSlice + c;
+          const uint32_t aph = (uint32_t)(r * kChunksPerSlice + c) & 1u;
+          // the W buffer is waited for at its first use in a slice only
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&bk.a_ready[g]), aph, abort_flag, kWaitLimitNs) &&
+                              (!fresh[g] ||
+                               mbar_wait(smem_u32(&bk.full_b[j]), (uint32_t)(loads[g] - 1) & 1u,
+                                         abort_flag, kWaitLimitNs)));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a = tmem + (uint32_t)g * kWGCols + aph * kACols;
+          const uint32_t d = tmem + (uint32_t)g * kWGCols + 2 * kACols;
+          const uint32_t bb = smem_u32(b_smem(j));
+#pragma unroll
+          for (int q = 0; q < 4; ++q)  // x1 against [0 | w0 | w1 | w2]
+            umma_bf16_ts_warp(d, a + 32 + 8 * q, smem_desc_sw128(bb + 32 * q), kIdesc, q > 0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)  // x0 against [w0 | w1 | w2 | w3]
+            umma_bf16_ts_warp(d, a + 8 * q,
+                              smem_desc_sw128(bb + kLimbRowOffset * kRowBytes + 32 * q), kIdesc, 1);
+          umma_commit_warp(smem_u32(&bk.d_ready[g]));
+          if (last_use[g]) umma_commit_warp(smem_u32(&bk.empty_b[j]));
+        }
+      }
+    }
+    if (!ok && lane == 0) fail(bk, err);
+    umma_commit_warp(smem_u32(&bk.drain));
+    mbar_wait(smem_u32(&bk.drain), 0, never, kDrainLimitNs);
   } else {
     // ---------------- compute warpgroups: one thread per tile row
     const int g = (warp - kFirstComputeWarp) >> 2;
@@ -358,17 +430,19 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     auto transform = [&](int k, float& tsq) -> bool {
       const int r = k / kChunksPerSlice, c = k % kChunksPerSlice;
       const int act = min(kWG, n - kWG * r);
-      const int i = seq_index(r, c, g, act);
+      // x stage of this chunk: rounds before r loaded kWG * kChunksPerSlice /
+      // kChunksPerStage stages each
+      const int i = r * kWG * (kChunksPerSlice / kChunksPerStage) + (c / kChunksPerStage) * act + g;
       const int st = i % kXStages;
       const uint32_t ph = (uint32_t)(i / kXStages) & 1u;
       bool ok = mbar_wait(smem_u32(&bk.full_x[st]), ph, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) return false;
-      const uint8_t* xt = x_smem(st);
+      const uint32_t xt = smem_u32(x_smem(st)) + (uint32_t)(c % kChunksPerStage) * kXChunkBytes;
       uint32_t xw[32];
 #pragma unroll
       for (int p = 0; p < 8; ++p) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xt + xoff[p]);
+        const uint4 v = lds128(xt + xoff[p]);
         xw[4 * p] = v.x; xw[4 * p + 1] = v.y; xw[4 * p + 2] = v.z; xw[4 * p + 3] = v.w;
       }
       tsq = sq_tree64_f32x2(xw);
@@ -377,21 +451,22 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       // puts x on the grid); x1 = x - x0 is exact.  Both are bf16, <= 8 bits.
       const uint32_t magic = bf16x2_split_magic(xw);
       const uint32_t a_col = a_base + (uint32_t)(k & 1) * kACols;
+      {
+        uint32_t w0[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t w0[16], w1[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const uint32_t wd = xw[16 * half + t];
-          w0[t] = bf16x2_sub(bf16x2_fma(wd, kBf16x2One, magic), magic);
-          w1[t] = bf16x2_sub(wd, w0[t]);
+        for (int t = 0; t < 32; ++t) {
+          w0[t] = bf16x2_sub(bf16x2_fma(xw[t], kBf16x2One, magic), magic);
+          xw[t] = bf16x2_sub(xw[t], w0[t]);  // x1, in place
         }
-        tmem_st16(lanes | (a_col + 16 * half), w0);
-        tmem_st16(lanes | (a_col + 32 + 16 * half), w1);
+        // the stores complete in the background; tcgen05.wait::st comes
+        // before the A buffer is handed to the MMA warp
+        tmem_st32(lanes | a_col, w0);
+        tmem_st32(lanes | (a_col + 32), xw);
       }
-      tmem_wait_st();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bk.empty_x[st]));  // x tile read
+      if (c % kChunksPerStage == kChunksPerStage - 1) {  // both chunks of the stage read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bk.empty_x[st]));
+      }
       return true;
     };
 
@@ -401,6 +476,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     float sqs = 0.0f, tsq_cur = 0.0f, tsq_next = 0.0f;
     bool ok = my_chunks > 0 ? transform(0, tsq_cur) : true;
     if (ok && my_chunks > 0) {
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bk.a_ready[g]));
@@ -414,45 +490,35 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // D = [top | r1 | r2 | r3]; chunk dot = top + ((r1 + r2) + r3), in output pairs
+      // D = [top | r1 | r2 | r3]; chunk dot = top + ((r1 + r2) + r3), in output
+      // pairs; all 96 columns in one TMEM round trip
       {
-        uint32_t rr[3][kMix];
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          tmem_ld16(lanes | (d_col + 24 * (q + 1)), rr[q]);
-          tmem_ld8(lanes | (d_col + 24 * (q + 1) + 16), rr[q] + 16);
-        }
-        tmem_wait_ld();
-        float2 rest[kMix / 2];
-#pragma unroll
-        for (int j = 0; j < kMix / 2; ++j) {
-          const float2 u = make_float2(__uint_as_float(rr[0][2 * j]), __uint_as_float(rr[0][2 * j + 1]));
-          const float2 v = make_float2(__uint_as_float(rr[1][2 * j]), __uint_as_float(rr[1][2 * j + 1]));
-          const float2 w = make_float2(__uint_as_float(rr[2][2 * j]), __uint_as_float(rr[2][2 * j + 1]));
-          rest[j] = __fadd2_rn(__fadd2_rn(u, v), w);
-        }
-        uint32_t top[kMix];
-        tmem_ld16(lanes | d_col, top);
-        tmem_ld8(lanes | (d_col + 16), top + 16);
+        uint32_t dv[4 * kMix];
+        tmem_ld32(lanes | d_col, dv);
+        tmem_ld32(lanes | (d_col + 32), dv + 32);
+        tmem_ld32(lanes | (d_col + 64), dv + 64);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < kMix / 2; ++j) {
-          const float2 d = __fadd2_rn(
-              make_float2(__uint_as_float(top[2 * j]), __uint_as_float(top[2 * j + 1])), rest[j]);
-          acc[j] = __fadd2_rn(acc[j], d);
+          const float2 top = make_float2(__uint_as_float(dv[2 * j]), __uint_as_float(dv[2 * j + 1]));
+          const float2 u = make_float2(__uint_as_float(dv[kMix + 2 * j]), __uint_as_float(dv[kMix + 2 * j + 1]));
+          const float2 v = make_float2(__uint_as_float(dv[2 * kMix + 2 * j]), __uint_as_float(dv[2 * kMix + 2 * j + 1]));
+          const float2 w = make_float2(__uint_as_float(dv[3 * kMix + 2 * j]), __uint_as_float(dv[3 * kMix + 2 * j + 1]));
+          acc[j] = __fadd2_rn(acc[j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
         }
       }
       sqs = __fadd_rn(sqs, tsq_cur);
       tsq_cur = tsq_next;
       // A(k+1) is written and D has been read: the MMAs of chunk k+1 may run
       if (k + 1 < my_chunks) {
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bk.a_ready[g]));
       }
       if (k % kChunksPerSlice == kChunksPerSlice - 1) {
         const int64_t unit = u_begin + kWG * (k / kChunksPerSlice) + g;
-        const int tile = (int)(unit / n_slices), s = (int)(unit % n_slices);
+        const int tile = unit_tile(unit), s = unit_slice(unit);
         float* p = part + (int64_t)s * kPartStride * Mpad + (int64_t)tile * kTileM + row;
 #pragma unroll
         for (int j = 0; j < kMix / 2; ++j) {
@@ -513,6 +579,25 @@ inline bool make_map_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view of a row-major bf16 matrix [rows, inner] as [inner / 64 chunks]
+// [rows][64]: one box is `box_chunks` consecutive 64-column chunks of
+// `box_rows` rows, stored in shared memory as box_chunks [box_rows x 128 B]
+// tiles with the 128-byte swizzle; reads past the rows return zeros.
+inline bool make_map_bf16_3d_chunks(CUtensorMap* map, const void* base, uint64_t inner,
+                                    uint64_t rows, uint64_t row_bytes, uint32_t box_rows,
+                                    uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kChunk, rows, inner / kChunk};
+  const cuuint64_t strides[2] = {row_bytes, (cuuint64_t)kChunk * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kChunk, box_rows, box_chunks};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+            box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 
 // Packs W into limbs, then runs the tensor-core contraction into `part`.
@@ -526,8 +611,8 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
   if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
 
   CUtensorMap mx, mw;
-  if (!tc::make_map_bf16_2d(&mx, x, (uint64_t)K, (uint64_t)M, (uint64_t)x_stride * 2, kChunk,
-                            tc::kTileM) ||
+  if (!tc::make_map_bf16_3d_chunks(&mx, x, (uint64_t)K, (uint64_t)M, (uint64_t)x_stride * 2,
+                                    tc::kTileM, tc::kChunksPerStage) ||
       !tc::make_map_bf16_2d(&mw, limbs, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
                             tc::kLimbRows))
     return HCMIX_ERR_CUDA;
@@ -543,7 +628,7 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
                            (int)tc::kSmemBytes) != cudaSuccess)
     return HCMIX_ERR_CUDA;
   tc::hcmix_tc_kernel<<<(unsigned)grid, tc::kThreads, tc::kSmemBytes, stream>>>(
-      mx, mw, (int)(K / kSlice), Mpad, n_units, part, err);
+      mx, mw, (int)n_tiles, Mpad, n_units, part, err);
   return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
 }
 
