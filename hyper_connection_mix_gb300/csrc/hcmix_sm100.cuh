@@ -19,6 +19,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start once every CTA of the grid before it in the stream
+// has issued grid_launch_dependents (or exited); grid_dependency_wait then
+// blocks the calling thread until that earlier grid has completed and its
+// memory is visible.  Without such an earlier grid both return at once.
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- shared memory
 // Explicit shared-space accesses on 32-bit shared addresses (a pointer that
 // went through an integer cast would otherwise be accessed generically).

@@ -108,6 +108,7 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
 __global__ void __launch_bounds__(kPackThreads)
 hcmix_pack_limbs_kernel(const float* __restrict__ W, int64_t w_stride, int K,
                         uint16_t* __restrict__ limbs) {
+  sm100::grid_launch_dependents();  // the contraction may start streaming x now
   const int sub = threadIdx.x & 15;
   const int task = blockIdx.x * kPackTasksPerBlock + (threadIdx.x >> 4);
   const int nch = K / kChunk;
@@ -301,6 +302,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // last use)
     if (lane == 0) {
       prefetch_tensormap(&tmap_w);
+      grid_dependency_wait();  // the limbs come from the pack kernel launched before
       const uint64_t pol = l2_policy_evict_last();
       int loads[kWG] = {0, 0}, cur[kWG] = {-1, -1};
       bool ok = true;
@@ -627,8 +629,21 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
   if (cudaFuncSetAttribute(tc::hcmix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kSmemBytes) != cudaSuccess)
     return HCMIX_ERR_CUDA;
-  tc::hcmix_tc_kernel<<<(unsigned)grid, tc::kThreads, tc::kSmemBytes, stream>>>(
-      mx, mw, (int)n_tiles, Mpad, n_units, part, err);
+  // launched as a programmatic dependent of the pack kernel: x streams while
+  // the limbs are being written; the W producer waits for them
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(tc::kThreads);
+  cfg.dynamicSmemBytes = tc::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, tc::hcmix_tc_kernel, mx, mw, (int)n_tiles, Mpad, n_units, part,
+                         err) != cudaSuccess)
+    return HCMIX_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
 }
 
