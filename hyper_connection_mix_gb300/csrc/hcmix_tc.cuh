@@ -494,30 +494,29 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       tc_fence_after();
       // D = [top | r1 | r2 | r3]; chunk dot = top + ((r1 + r2) + r3), in output
       // pairs; all 96 columns in one TMEM round trip
-      {
-        uint32_t dv[4 * kMix];
-        tmem_ld32(lanes | d_col, dv);
-        tmem_ld32(lanes | (d_col + 32), dv + 32);
-        tmem_ld32(lanes | (d_col + 64), dv + 64);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < kMix / 2; ++j) {
-          const float2 top = make_float2(__uint_as_float(dv[2 * j]), __uint_as_float(dv[2 * j + 1]));
-          const float2 u = make_float2(__uint_as_float(dv[kMix + 2 * j]), __uint_as_float(dv[kMix + 2 * j + 1]));
-          const float2 v = make_float2(__uint_as_float(dv[2 * kMix + 2 * j]), __uint_as_float(dv[2 * kMix + 2 * j + 1]));
-          const float2 w = make_float2(__uint_as_float(dv[3 * kMix + 2 * j]), __uint_as_float(dv[3 * kMix + 2 * j + 1]));
-          acc[j] = __fadd2_rn(acc[j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
-        }
-      }
-      sqs = __fadd_rn(sqs, tsq_cur);
-      tsq_cur = tsq_next;
+      uint32_t dv[4 * kMix];
+      tmem_ld32(lanes | d_col, dv);
+      tmem_ld32(lanes | (d_col + 32), dv + 32);
+      tmem_ld32(lanes | (d_col + 64), dv + 64);
+      tmem_wait_ld();
       // A(k+1) is written and D has been read: the MMAs of chunk k+1 may run
+      // while this chunk's dot is formed
       if (k + 1 < my_chunks) {
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bk.a_ready[g]));
       }
+#pragma unroll
+      for (int j = 0; j < kMix / 2; ++j) {
+        const float2 top = make_float2(__uint_as_float(dv[2 * j]), __uint_as_float(dv[2 * j + 1]));
+        const float2 u = make_float2(__uint_as_float(dv[kMix + 2 * j]), __uint_as_float(dv[kMix + 2 * j + 1]));
+        const float2 v = make_float2(__uint_as_float(dv[2 * kMix + 2 * j]), __uint_as_float(dv[2 * kMix + 2 * j + 1]));
+        const float2 w = make_float2(__uint_as_float(dv[3 * kMix + 2 * j]), __uint_as_float(dv[3 * kMix + 2 * j + 1]));
+        acc[j] = __fadd2_rn(acc[j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
+      }
+      sqs = __fadd_rn(sqs, tsq_cur);
+      tsq_cur = tsq_next;
       if (k % kChunksPerSlice == kChunksPerSlice - 1) {
         const int64_t unit = u_begin + kWG * (k / kChunksPerSlice) + g;
         const int tile = unit_tile(unit), s = unit_slice(unit);
