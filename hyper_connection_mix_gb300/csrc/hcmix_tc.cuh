@@ -520,14 +520,17 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       if (k % kChunksPerSlice == kChunksPerSlice - 1) {
         const int64_t unit = u_begin + kWG * (k / kChunksPerSlice) + g;
         const int tile = unit_tile(unit), s = unit_slice(unit);
+        // the reduce kernel reads the partials next: keep them in L2 while x
+        // streams through it with evict_first
         float* p = part + (int64_t)s * kPartStride * Mpad + (int64_t)tile * kTileM + row;
+        const uint64_t keep = l2_policy_evict_last();
 #pragma unroll
         for (int j = 0; j < kMix / 2; ++j) {
-          p[(int64_t)(2 * j) * Mpad] = acc[j].x;
-          p[(int64_t)(2 * j + 1) * Mpad] = acc[j].y;
+          stg_f32_hint(p + (int64_t)(2 * j) * Mpad, acc[j].x, keep);
+          stg_f32_hint(p + (int64_t)(2 * j + 1) * Mpad, acc[j].y, keep);
           acc[j] = make_float2(0.0f, 0.0f);
         }
-        p[(int64_t)kMix * Mpad] = sqs;
+        stg_f32_hint(p + (int64_t)kMix * Mpad, sqs, keep);
         sqs = 0.0f;
       }
     }
