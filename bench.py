@@ -18,6 +18,10 @@ Our arm prints one JSON line with:
   cpu_baseline  the CPU oracle on the same workload (rank 0, N = 1 only);
   clocks     nvidia-smi samples taken during the timed region.
 `--impl reference` times the CPU oracle instead (bounded row samples per step).
+`--sweep` times the other workloads instead, one JSON line each: the decode
+sweep M in {1, 4, 16, 64, 128, 256} on both paths, M = 512 with outlier
+channels, and one 86-call forward (M = 16384, distinct W / scale / base per
+call) replayed from a single CUDA graph.
 Multi-GPU (torchrun): each rank runs its own 4096 rows (weak scaling, rows are
 independent, no collective on the data path).
 """
@@ -58,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--path", choices=("auto", "simt", "tc"), default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the other workloads (one JSON line each) instead of the headline")
     return ap.parse_args(argv)
 
 
@@ -392,11 +398,107 @@ def run_ours(args, rank, world, local):
         dist.destroy_process_group()
 
 
+def graph_us(fn, stream, replays: int, warmup: int = 5) -> float:
+    """Device time per replay of a CUDA graph holding fn(), in µs."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(replays):
+            g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / replays
+
+
+def run_sweep(args):
+    """The decode sweep, the outlier config and the 86-call forward."""
+    import numpy as np
+    import torch
+
+    import hcmix_inputs as hi
+    from hyper_connection_mix_gb300 import binding, traffic
+
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device)
+    dev = lambda a: torch.from_numpy(a).to(device)
+    W, sc, bs = dev(hi.make_w()), dev(hi.make_scale()), dev(hi.make_base())
+
+    def fused_case(x, path, calls=100):
+        M, K = x.shape
+        ws = binding.alloc_workspace(M, K, device)
+        out = (torch.empty(M, 4, device=device), torch.empty(M, 4, device=device),
+               torch.empty(M, 4, 4, device=device))
+
+        def fn():  # `calls` back-to-back calls per graph, as a decode loop issues them
+            for _ in range(calls):
+                binding.hc_mix_fused(x, W, sc, bs, ITERS, RMS_EPS, HC_EPS, out=out, workspace=ws,
+                                     stream=stream, path=path)
+        return graph_us(fn, stream, replays=10) / calls
+
+    x256 = hi.make_x(256)
+    for M in (1, 4, 16, 64, 128, 256):
+        x = torch.from_numpy(np.ascontiguousarray(x256[:M]).view(np.int16)).view(
+            torch.bfloat16).to(device)
+        for path in ("simt", "tc"):
+            us = fused_case(x, path)
+            gbs = traffic.algorithmic_bytes(M, K_COLS) / (us * 1e-6) / 1e9
+            print(json.dumps({"config": f"decode M={M} K={K_COLS}", "path": path,
+                              "us_per_call": us, "hbm_gbs": gbs,
+                              "auto_path": binding.hc_mix_auto_path(M)}), flush=True)
+    x = torch.from_numpy(hi.make_x(512, outliers=True).view(np.int16)).view(
+        torch.bfloat16).to(device)
+    us = fused_case(x, "auto", calls=20)
+    print(json.dumps({"config": f"M=512 outliers K={K_COLS}", "path": binding.hc_mix_auto_path(512),
+                      "us_per_call": us,
+                      "hbm_gbs": traffic.algorithmic_bytes(512, K_COLS) / (us * 1e-6) / 1e9}),
+          flush=True)
+
+    # 86 calls per forward (43 layers x 2), M = 16384, one shared x, distinct
+    # W / scale / base per call (the stack test's seeds), one CUDA graph
+    M, K, calls = 16384, K_COLS, 86
+    x = torch.from_numpy(hi.make_x(M).view(np.int16)).view(torch.bfloat16).to(device)
+    Ws, scs, bss = [], [], []
+    for i in range(calls):
+        s_w, s_s, s_b = hi.layer_seeds(i)
+        Ws.append(dev(hi.make_w(seed=s_w)))
+        scs.append(dev(hi.make_scale(seed=s_s)))
+        bss.append(dev(hi.make_base(seed=s_b)))
+    ws = binding.alloc_workspace(M, K, device)
+    outs = [(torch.empty(M, 4, device=device), torch.empty(M, 4, device=device),
+             torch.empty(M, 4, 4, device=device)) for _ in range(calls)]
+
+    def forward():
+        for i in range(calls):
+            binding.hc_mix_fused(x, Ws[i], scs[i], bss[i], ITERS, RMS_EPS, HC_EPS, out=outs[i],
+                                 workspace=ws, stream=stream, path="auto")
+    us = graph_us(forward, stream, replays=5, warmup=2)
+    per_call = traffic.algorithmic_bytes(M, K)
+    print(json.dumps({"config": f"86-call forward M={M} K={K} (CUDA graph)",
+                      "path": binding.hc_mix_auto_path(M), "us_per_forward": us,
+                      "us_per_call": us / calls,
+                      "hbm_gbs": calls * per_call / (us * 1e-6) / 1e9,
+                      "roofline_us_at_8tbs": calls * per_call / 8e12 * 1e6}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     rank, world, local = dist_env()
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

@@ -58,12 +58,13 @@ typedef enum {
   HCMIX_ERR_DEVICE = 6       /* a kernel recorded an error (see hc_mix_device_status) */
 } hcmix_status;
 
-/* Which contraction kernel runs.  AUTO picks by M; the others force one path
- * (both give results within the stated tolerance of each other). */
+/* Which contraction kernel runs.  AUTO picks by M (hc_mix_auto_path; on
+ * GB300 the tensor-core kernel at every M); the others force one path (both
+ * give results within the stated tolerance of each other). */
 typedef enum {
   HCMIX_PATH_AUTO = 0,
-  HCMIX_PATH_SIMT = 1,  /* CUDA-core split-K kernel (small M) */
-  HCMIX_PATH_TC = 2     /* tcgen05 tensor-core kernel (large M) */
+  HCMIX_PATH_SIMT = 1,  /* CUDA-core split-K kernel */
+  HCMIX_PATH_TC = 2     /* tcgen05 tensor-core kernel */
 } hcmix_path;
 
 /* Bytes of device workspace that hc_mix_stats / hc_mix_fused need for M rows.
