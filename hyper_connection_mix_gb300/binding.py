@@ -129,7 +129,7 @@ def hc_mix_stats(x: torch.Tensor, W: torch.Tensor, mix_out=None, sq_out=None, wo
     workspace = alloc_workspace(M, K, x.device) if workspace is None else workspace
     st = lib().hc_mix_stats_ex(_ptr(x), x.stride(0), _ptr(W), W.stride(0), M, K, W.shape[0],
                                _ptr(mix_out), _ptr(sq_out), _ptr(workspace), workspace.numel(),
-                               _stream(stream), PATHS[path])
+                               _stream(stream), PATHS[_auto(path, x.device)])
     _check(st, "hc_mix_stats")
     return mix_out, sq_out
 
@@ -172,7 +172,8 @@ def hc_mix_fused(x: torch.Tensor, W: torch.Tensor, hc_scale: torch.Tensor,
     st = lib().hc_mix_fused_ex(_ptr(x), x.stride(0), _ptr(W), W.stride(0), M, K, W.shape[0], HC,
                                _ptr(hc_scale), _ptr(hc_base), sinkhorn_iters, rms_eps, hc_eps,
                                _ptr(pre), _ptr(post), _ptr(comb), _ptr(mix_out), _ptr(sq_out),
-                               _ptr(workspace), workspace.numel(), _stream(stream), PATHS[path])
+                               _ptr(workspace), workspace.numel(), _stream(stream),
+                               PATHS[_auto(path, x.device)])
     _check(st, "hc_mix_fused")
     return out
 
@@ -184,12 +185,64 @@ def hc_mix_contract(x: torch.Tensor, W: torch.Tensor, workspace: torch.Tensor, s
     M, K = x.shape
     st = lib().hc_mix_contract_ex(_ptr(x), x.stride(0), _ptr(W), W.stride(0), M, K, W.shape[0],
                                   _ptr(workspace), workspace.numel(), _stream(stream),
-                                  PATHS[path])
+                                  PATHS[_auto(path, x.device)])
     _check(st, "hc_mix_contract")
 
 
 def hc_mix_auto_path(M: int) -> str:
     return {v: k for k, v in PATHS.items()}[int(lib().hc_mix_auto_path(M))]
+
+
+# ---------------------------------------------------------------- self-check
+
+_self_checked: dict = {}
+
+
+def self_check(device=None, M: int = 200, K: int = 1024) -> dict:
+    """Runs both contraction kernels on small seeded inputs and compares them.
+
+    Two independent GPU implementations (the tcgen05 tensor-core kernel and
+    the CUDA-core split-K kernel) must agree on mix and sq within the path's
+    tolerance (|a - b| <= max(2e-6 |b|, 1e-6)); on integer-valued inputs, where
+    every partial sum is an integer below 2^24, both must give the exact
+    product.  Returns {"ok": bool, "max_ratio": worst |a - b| / tolerance,
+    "integer_exact": bool}.  Synchronises the device; not for use during
+    CUDA-graph capture.
+    """
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(12345)
+    x = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
+    x[:, ::97] *= 20  # a few outlier channels
+    W = torch.randn(MIX, K, generator=g, device=dev) * K ** -0.5
+    mt, st = hc_mix_stats(x, W, path="tc")
+    ms, ss = hc_mix_stats(x, W, path="simt")
+    ratio = 0.0
+    for a, b in ((mt, ms), (st, ss)):
+        tol = torch.clamp(2e-6 * b.abs(), min=1e-6)
+        ratio = max(ratio, float(((a - b).abs() / tol).max()))
+    xi = torch.randint(-4, 5, (M, K), generator=g, device=dev)
+    wi = torch.randint(-8, 9, (MIX, K), generator=g, device=dev)
+    exact = (xi.double() @ wi.double().T).float()
+    ok_int = True
+    for path in ("tc", "simt"):
+        mi, _ = hc_mix_stats(xi.to(torch.bfloat16), wi.float(), path=path)
+        ok_int = ok_int and bool(torch.equal(mi, exact))
+    torch.cuda.synchronize(dev)
+    return {"ok": ratio <= 1.0 and ok_int, "max_ratio": ratio, "integer_exact": ok_int}
+
+
+def _auto(path: str, device: torch.device) -> str:
+    """With HCMIX_SELF_CHECK=1, the first AUTO call on a device runs self_check
+    and keeps to the CUDA-core kernel if the tensor-core kernel disagrees."""
+    if path != "auto" or os.environ.get("HCMIX_SELF_CHECK") != "1":
+        return path
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    if idx not in _self_checked:
+        if torch.cuda.is_current_stream_capturing():
+            return path
+        _self_checked[idx] = self_check(torch.device("cuda", idx))
+    return "auto" if _self_checked[idx]["ok"] else "simt"
 
 
 def hc_mix_device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -111,3 +111,18 @@ def test_fused_and_sinkhorn_validation(L):
 def test_device_status_rejects_bad_workspace(L):
     assert L.hc_mix_device_status(None, None) == 1
     assert L.hc_mix_device_status(0x100080, None) == 1
+
+
+def test_self_check_dispatch(monkeypatch):
+    """AUTO keeps to the CUDA-core kernel on a device whose self-check failed,
+    only when HCMIX_SELF_CHECK=1; forced paths are never changed."""
+    import torch
+    d = torch.device("cuda", 0)
+    monkeypatch.delenv("HCMIX_SELF_CHECK", raising=False)
+    assert binding._auto("auto", d) == "auto"
+    monkeypatch.setenv("HCMIX_SELF_CHECK", "1")
+    monkeypatch.setitem(binding._self_checked, 0, {"ok": False})
+    assert binding._auto("auto", d) == "simt"
+    assert binding._auto("tc", d) == "tc"
+    monkeypatch.setitem(binding._self_checked, 0, {"ok": True})
+    assert binding._auto("auto", d) == "auto"

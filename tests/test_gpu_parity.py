@@ -261,3 +261,15 @@ def test_stack86_m16384_sampled():
         assert np.all(comb > 0)
         assert np.max(np.abs(comb.sum(1) - 1)) < 1e-5
     assert binding.hc_mix_device_status(ws) == 0
+
+
+@pytest.mark.gpu
+def test_self_check_paths_agree():
+    """The first-call self-check: both contraction kernels agree on seeded and
+    integer-valued inputs."""
+    if not (path_available("simt") and path_available("tc")):
+        pytest.skip("both paths needed")
+    rep = binding.self_check()
+    assert rep["ok"], rep
+    assert rep["integer_exact"]
+    assert rep["max_ratio"] <= 1.0
