@@ -20,7 +20,8 @@ Our arm prints one JSON line with:
 `--impl reference` times the CPU oracle instead (bounded row samples per step).
 `--sweep` times the other workloads instead, one JSON line each: the decode
 sweep M in {1, 4, 16, 64, 128, 256} on both paths, M = 512 with outlier
-channels, and one 86-call forward (M = 16384, distinct W / scale / base per
+channels, the stock split-K / fused full-K A/B at M in {512, 1024, 2048, 4096},
+and one 86-call forward (M = 16384, distinct W / scale / base per
 call) replayed from a single CUDA graph.
 Multi-GPU (torchrun): each rank runs its own 4096 rows (weak scaling, rows are
 independent, no collective on the data path).
@@ -421,7 +422,8 @@ def graph_us(fn, stream, replays: int, warmup: int = 5) -> float:
 
 
 def run_sweep(args):
-    """The decode sweep, the outlier config and the 86-call forward."""
+    """The decode sweep, the outlier config, the split-K / full-K A/B and the
+    86-call forward."""
     import numpy as np
     import torch
 
@@ -462,6 +464,22 @@ def run_sweep(args):
                       "us_per_call": us,
                       "hbm_gbs": traffic.algorithmic_bytes(512, K_COLS) / (us * 1e-6) / 1e9}),
           flush=True)
+
+    # The page's A/B of its two designs at prefill sizes (its table: rows,
+    # stock split-K -> fused full-K, us per call), here on the same CUDA-core
+    # arithmetic, with the tensor-core split-K path beside them.
+    designs = {"simt": "stock split-K (CUDA cores)", "simt_fullk": "fused full-K (CUDA cores)",
+               "tc": "split-K (tensor cores)"}
+    x4096 = hi.make_x(4096)
+    for M in (512, 1024, 2048, 4096):
+        x = torch.from_numpy(np.ascontiguousarray(x4096[:M]).view(np.int16)).view(
+            torch.bfloat16).to(device)
+        for path, design in designs.items():
+            us = fused_case(x, path, calls=10)
+            print(json.dumps({"config": f"A/B M={M} K={K_COLS}", "path": path, "design": design,
+                              "us_per_call": us,
+                              "hbm_gbs": traffic.algorithmic_bytes(M, K_COLS) / (us * 1e-6) / 1e9}),
+                  flush=True)
 
     # 86 calls per forward (43 layers x 2), M = 16384, one shared x, distinct
     # W / scale / base per call (the stack test's seeds), one CUDA graph

@@ -96,6 +96,11 @@ hcmix_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
 }
 
+bool valid_path(hcmix_path path) {
+  return path == HCMIX_PATH_AUTO || path == HCMIX_PATH_SIMT || path == HCMIX_PATH_TC ||
+         path == HCMIX_PATH_SIMT_FULLK;
+}
+
 hcmix_path resolve_path(hcmix_path path, int64_t M) {
   if (path == HCMIX_PATH_AUTO) return M <= kSimtMaxRows ? HCMIX_PATH_SIMT : HCMIX_PATH_TC;
   return path;
@@ -115,6 +120,12 @@ hcmix_status launch_contraction(const void* x, int64_t x_stride, const float* W,
         static_cast<const uint16_t*>(x), x_stride, W, w_stride, (int)M, (int)ws.Mpad, part);
     return launch_status();
   }
+  if (path == HCMIX_PATH_SIMT_FULLK) {
+    hcmix_simt_fullk_kernel<<<(unsigned)((M + kSimtRows - 1) / kSimtRows), kSimtThreads, 0,
+                              stream>>>(static_cast<const uint16_t*>(x), x_stride, W, w_stride,
+                                        (int)M, (int)ws.Mpad, (int)ws.n_slices, part);
+    return launch_status();
+  }
   if (path == HCMIX_PATH_TC) {
     return tc_launch(static_cast<const uint16_t*>(x), x_stride, W, w_stride, M, K,
                      reinterpret_cast<uint16_t*>(base + ws.limbs_off), part, (int)ws.Mpad,
@@ -123,17 +134,21 @@ hcmix_status launch_contraction(const void* x, int64_t x_stride, const float* W,
   return HCMIX_ERR_INVALID_ARG;
 }
 
+// Ordered reduce of the stored slices (the full-K kernel stores one) and,
+// with do_epilogue, the epilogue.
 hcmix_status launch_reduce(int64_t M, int64_t K, void* workspace, const float* hc_scale,
                            const float* hc_base, int iters, float rms_eps, float hc_eps,
                            float* pre, float* post, float* comb, float* mix_out, float* sq_out,
-                           int do_epilogue, cudaStream_t stream) {
+                           int do_epilogue, cudaStream_t stream, hcmix_path path) {
   const Workspace ws = workspace_layout(M, K);
+  const int stored_slices =
+      resolve_path(path, M) == HCMIX_PATH_SIMT_FULLK ? 1 : (int)ws.n_slices;
   const float* part =
       reinterpret_cast<const float*>(static_cast<const char*>(workspace) + ws.part_off);
   const float inv_k = (float)(1.0 / (double)K);
   dim3 grid((unsigned)((M + kReduceRows - 1) / kReduceRows));
   hcmix_reduce_kernel<<<grid, kReduceThreads, 0, stream>>>(
-      part, (int)ws.n_slices, (int)ws.Mpad, (int)M, inv_k, hc_scale, hc_base, iters, rms_eps,
+      part, stored_slices, (int)ws.Mpad, (int)M, inv_k, hc_scale, hc_base, iters, rms_eps,
       hc_eps, pre, post, comb, mix_out, sq_out, do_epilogue);
   return launch_status();
 }
@@ -159,15 +174,14 @@ hcmix_status hc_mix_stats_ex(const void* x, int64_t x_stride, const float* W, in
   hcmix_status st = check_stats_args(x, x_stride, W, w_stride, M, K, mix, workspace,
                                      workspace_bytes);
   if (st != HCMIX_OK) return st;
-  if (path != HCMIX_PATH_AUTO && path != HCMIX_PATH_SIMT && path != HCMIX_PATH_TC)
-    return HCMIX_ERR_INVALID_ARG;
+  if (!valid_path(path)) return HCMIX_ERR_INVALID_ARG;
   if (M == 0) return HCMIX_OK;
   if (mix_out == nullptr || sq_out == nullptr) return HCMIX_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launch_contraction(x, x_stride, W, w_stride, M, K, workspace, s, path);
   if (st != HCMIX_OK) return st;
   return launch_reduce(M, K, workspace, nullptr, nullptr, 0, 0.f, 0.f, nullptr, nullptr, nullptr,
-                       mix_out, sq_out, 0, s);
+                       mix_out, sq_out, 0, s, path);
 }
 
 hcmix_status hc_mix_contract_ex(const void* x, int64_t x_stride, const float* W,
@@ -177,8 +191,7 @@ hcmix_status hc_mix_contract_ex(const void* x, int64_t x_stride, const float* W,
   hcmix_status st = check_stats_args(x, x_stride, W, w_stride, M, K, mix, workspace,
                                      workspace_bytes);
   if (st != HCMIX_OK) return st;
-  if (path != HCMIX_PATH_AUTO && path != HCMIX_PATH_SIMT && path != HCMIX_PATH_TC)
-    return HCMIX_ERR_INVALID_ARG;
+  if (!valid_path(path)) return HCMIX_ERR_INVALID_ARG;
   if (M == 0) return HCMIX_OK;
   return launch_contraction(x, x_stride, W, w_stride, M, K, workspace,
                             static_cast<cudaStream_t>(stream), path);
@@ -220,14 +233,13 @@ hcmix_status hc_mix_fused_ex(const void* x, int64_t x_stride, const float* W, in
   if (st != HCMIX_OK) return st;
   st = check_epilogue_args(M, K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
   if (st != HCMIX_OK) return st;
-  if (path != HCMIX_PATH_AUTO && path != HCMIX_PATH_SIMT && path != HCMIX_PATH_TC)
-    return HCMIX_ERR_INVALID_ARG;
+  if (!valid_path(path)) return HCMIX_ERR_INVALID_ARG;
   if (M == 0) return HCMIX_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launch_contraction(x, x_stride, W, w_stride, M, K, workspace, s, path);
   if (st != HCMIX_OK) return st;
   return launch_reduce(M, K, workspace, hc_scale, hc_base, sinkhorn_iters, rms_eps, hc_eps, pre,
-                       post, comb, mix_out, sq_out, 1, s);
+                       post, comb, mix_out, sq_out, 1, s, path);
 }
 
 hcmix_status hc_mix_fused(const void* x, int64_t x_stride, const float* W, int64_t w_stride,

@@ -59,12 +59,21 @@ typedef enum {
 } hcmix_status;
 
 /* Which contraction kernel runs.  AUTO picks by M (hc_mix_auto_path; on
- * GB300 the tensor-core kernel at every M); the others force one path (both
- * give results within the stated tolerance of each other). */
+ * GB300 the tensor-core kernel at every M); the others force one path (all
+ * give results within the stated tolerance of each other).
+ *
+ * HCMIX_PATH_SIMT and HCMIX_PATH_SIMT_FULLK are the hc_fused page's two
+ * designs on the same CUDA-core arithmetic, kept as an A/B pair: the stock
+ * engine's split-K layout (one CTA per slice and row block, every slice's
+ * totals stored in the workspace, then an ordered reduce) against the page's
+ * fused kernel (one CTA per row block walks all of K and keeps the running
+ * total, so only the total is stored; the page's module docstring).  Their
+ * statistics are bit-identical. */
 typedef enum {
   HCMIX_PATH_AUTO = 0,
-  HCMIX_PATH_SIMT = 1,  /* CUDA-core split-K kernel */
-  HCMIX_PATH_TC = 2     /* tcgen05 tensor-core kernel */
+  HCMIX_PATH_SIMT = 1,       /* CUDA-core split-K kernel (stock layout) */
+  HCMIX_PATH_TC = 2,         /* tcgen05 tensor-core split-K kernel */
+  HCMIX_PATH_SIMT_FULLK = 3  /* CUDA-core full-K kernel (the page's fused design) */
 } hcmix_path;
 
 /* Bytes of device workspace that hc_mix_stats / hc_mix_fused need for M rows.
@@ -118,8 +127,8 @@ hcmix_status hc_mix_fused_ex(const void* x, int64_t x_stride, const float* W, in
                              hcmix_path path);
 
 /* The contraction phase alone (the dominant kernel of hc_mix_stats and
- * hc_mix_fused): writes the per-slice partial totals into the workspace and
- * nothing else.  Arguments as hc_mix_stats_ex.  For timing and profiling the
+ * hc_mix_fused): writes the per-slice partial totals (HCMIX_PATH_SIMT_FULLK:
+ * the one running total) into the workspace and nothing else.  Arguments as hc_mix_stats_ex.  For timing and profiling the
  * phase on its own stream position; the partials are not a public format. */
 hcmix_status hc_mix_contract_ex(const void* x, int64_t x_stride, const float* W,
                                 int64_t w_stride, int64_t M, int64_t K, int mix,

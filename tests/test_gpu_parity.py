@@ -17,7 +17,7 @@ from hyper_connection_mix_gb300 import binding
 pytestmark = pytest.mark.gpu
 
 THREADS = os.cpu_count() or 1
-PATHS = ("simt", "tc")
+PATHS = ("simt", "tc", "simt_fullk")
 
 
 def dev_x(x):
@@ -219,6 +219,22 @@ def test_paths_agree_on_overlapping_sizes():
     assert_mix_close(b[3], a[3].astype(np.float64), "simt vs tc")
     for u, v in zip(a[:3], b[:3]):
         assert np.max(np.abs(u - v)) <= 1e-5
+
+
+@pytest.mark.parametrize("M,K", [(37, 2048), (300, 20480)])
+def test_fullk_bit_identical_to_split_k(M, K):
+    """The page's fused design (one CTA walks all of K with a running total)
+    and the stock split-K layout (per-slice totals, then the ordered reduce)
+    add the same values in the same order, so every output is bit-identical."""
+    for p in ("simt", "simt_fullk"):
+        if not path_available(p):
+            pytest.fail(f"kernel path {p} is not available in this library")
+    x, W = hi.make_x(M, K=K, outliers=True), hi.make_w(K=K)
+    sc, bs = hi.make_scale(), hi.make_base()
+    a = run(x, W, sc, bs, "simt")
+    b = run(x, W, sc, bs, "simt_fullk")
+    for name, u, v in zip(("pre", "post", "comb", "mix", "sq"), a, b):
+        assert np.array_equal(u.view(np.uint32), v.view(np.uint32)), f"{name} differs"
 
 
 def test_stack86_m16384_sampled():
