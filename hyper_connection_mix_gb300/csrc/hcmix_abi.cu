@@ -33,7 +33,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Workspace {
   size_t err_off = 0;     // uint32 device error word (256-byte header)
-  size_t limbs_off = 0;   // bf16 W limbs [4][24][K] for the tensor-core path
+  size_t limbs_off = 0;   // packed W for the tensor-core path: bf16 limbs [4][24][K]
+                          // (exact) or fp32 tf32x3 parts [2][24][K], the same size
   size_t limbs_bytes = 0;
   size_t part_off = 0;    // fp32 partials [slices][25][Mpad]
   size_t part_bytes = 0;
@@ -98,7 +99,7 @@ hcmix_status launch_status() {
 
 bool valid_path(hcmix_path path) {
   return path == HCMIX_PATH_AUTO || path == HCMIX_PATH_SIMT || path == HCMIX_PATH_TC ||
-         path == HCMIX_PATH_SIMT_FULLK;
+         path == HCMIX_PATH_SIMT_FULLK || path == HCMIX_PATH_TC_TF32X3;
 }
 
 hcmix_path resolve_path(hcmix_path path, int64_t M) {
@@ -126,10 +127,11 @@ hcmix_status launch_contraction(const void* x, int64_t x_stride, const float* W,
                                         (int)M, (int)ws.Mpad, (int)ws.n_slices, part);
     return launch_status();
   }
-  if (path == HCMIX_PATH_TC) {
+  if (path == HCMIX_PATH_TC || path == HCMIX_PATH_TC_TF32X3) {
     return tc_launch(static_cast<const uint16_t*>(x), x_stride, W, w_stride, M, K,
-                     reinterpret_cast<uint16_t*>(base + ws.limbs_off), part, (int)ws.Mpad,
-                     reinterpret_cast<uint32_t*>(base + ws.err_off), stream);
+                     base + ws.limbs_off, part, (int)ws.Mpad,
+                     reinterpret_cast<uint32_t*>(base + ws.err_off), stream,
+                     path == HCMIX_PATH_TC_TF32X3);
   }
   return HCMIX_ERR_INVALID_ARG;
 }

@@ -189,6 +189,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int c
       : "memory");
 }
 
+// 4-D tiled bulk tensor load global -> shared (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, int c0, int c1, int c2,
+                                            int c3, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+      "l"(policy)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -304,6 +315,12 @@ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Instruction descriptor of tcgen05.mma kind::tf32: as idesc_bf16_f32 with
+// A and B tf32 (format 2 in bits 7-9 and 10-12).
+constexpr uint32_t idesc_tf32_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T, one elected thread, cta_group::1.
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
@@ -331,6 +348,20 @@ __device__ __forceinline__ void umma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tm
       : "memory");
 }
 
+// kind::tf32 counterpart of umma_bf16_ts_warp: A and B hold 32-bit elements
+// read as tf32, K = 8 per instruction.
+__device__ __forceinline__ void umma_tf32_ts_warp(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -347,6 +378,14 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 }
 
 // ---------------------------------------------------------------- packed arithmetic
+
+// fp32 -> tf32 (10 stored fraction bits), round to nearest with ties away from
+// zero; the result is an fp32 bit pattern whose low 13 bits are zero.
+__device__ __forceinline__ float cvt_rna_tf32(float v) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+  return __uint_as_float(r);
+}
 
 // max(|a|, |b|) per bf16 half (the sign of the result is not used).
 __device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {

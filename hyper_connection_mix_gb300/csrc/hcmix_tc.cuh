@@ -28,6 +28,17 @@
 // transforms chunk k+1 into its second TMEM A buffer before it waits for the
 // MMAs of chunk k, so the MMA latency hides behind the next transform; D is
 // released together with A(k+1).  TMEM holds 2 x (2 x 64 A + 96 D) columns.
+//
+// tf32x3 mode (hcmix_tc_kernel<true>): the hc_fused page's own chunk
+// arithmetic instead of the exact limbs.  W is packed as big = W rounded to
+// tf32 (nearest, ties away: the page's _tf32_rna) and small = W - big; x
+// (exact in tf32) goes to TMEM as fp32; per chunk the MMA warp issues, in the
+// page's order, dot(x, small) from zero and then dot(x, big) on top of it:
+// 2 x 8 MMAs of M=128, N=32 (24 outputs + 8 zero rows), K=8, kind::tf32, and
+// D's first 24 columns are the chunk dot.  The rest of the pipeline (units,
+// stages, barriers, sum of squares, partials) is the same.  The tensor
+// core's own rounding inside each MMA decides the last bits of every chunk
+// dot, so this mode is not exact; the page gives no bound either.
 #pragma once
 
 #include <cuda.h>
@@ -55,17 +66,13 @@ constexpr int kTileM = 128;
 constexpr uint32_t kRowBytes = 128;                       // 64 bf16 per smem row
 constexpr uint32_t kXChunkBytes = kTileM * kRowBytes;     // one chunk of a tile
 constexpr uint32_t kXBytes = kChunksPerStage * kXChunkBytes;  // x stage
-constexpr uint32_t kBRows = 120;                          // B rows the MMAs read
-constexpr uint32_t kBBytes = kBRows * kRowBytes;          // B buffer
+constexpr uint32_t kBRows = 120;                          // exact-mode B rows the MMAs read
 constexpr uint32_t kLimbRows = 4 * kMix;                  // w0..w3, 24 rows each
 constexpr uint32_t kLimbRowOffset = kMix;                 // limbs occupy B rows 24..119
 constexpr uint32_t kXTxBytes = kXBytes;
-constexpr uint32_t kBTxBytes = kLimbRows * kRowBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACols = 64;                           // x0: 32 columns, x1: 32 columns
-constexpr uint32_t kN = 96;
-constexpr uint32_t kWGCols = 2 * kACols + kN;             // two A buffers and one D per warpgroup
-constexpr uint32_t kIdesc = sm100::idesc_bf16_f32(128, kN);
+constexpr uint32_t kACols = 64;  // exact: x0 and x1, 32 columns each; tf32x3: 64 fp32 x
+constexpr uint32_t kTf32Rows = 32;  // tf32x3 B rows per part: 24 outputs + 8 zero rows
 constexpr uint64_t kWaitLimitNs = 2000000000ull;          // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 500000000ull;
 constexpr uint32_t kWarpArrivals = 4;                      // one arrive per warp of a warpgroup
@@ -83,14 +90,37 @@ struct Bookkeeping {
   int never;  // stays 0: the abort flag of waits that must not be cut short
 };
 
-constexpr size_t kRingBytes = (size_t)kXStages * kXBytes + (size_t)kBStages * kBBytes;
-constexpr size_t kSmemBytes = kRingBytes + 1024 + 1024;
+// Per-mode B buffer (one per chunk of a warpgroup's slice), MMA shape and
+// TMEM use.
+template <bool kTf32>
+struct Mode;
+template <>
+struct Mode<false> {  // exact limbs: 24 zero rows, then w0..w3 (96 rows), bf16
+  static constexpr uint32_t kBBytes = kBRows * kRowBytes;
+  static constexpr uint32_t kBTxBytes = kLimbRows * kRowBytes;
+  static constexpr uint32_t kN = 96;
+  static constexpr uint32_t kIdesc = sm100::idesc_bf16_f32(128, kN);
+};
+template <>
+struct Mode<true> {  // tf32x3: [big, small][two 32-column halves][32 rows][128 B], fp32
+  static constexpr uint32_t kBBytes = 2 * 2 * kTf32Rows * kRowBytes;
+  static constexpr uint32_t kBTxBytes = kBBytes;  // one TMA box, zero rows included
+  static constexpr uint32_t kN = kTf32Rows;
+  static constexpr uint32_t kIdesc = sm100::idesc_tf32_f32(128, kN);
+};
+template <bool kTf32>
+constexpr uint32_t kWGCols = 2 * kACols + Mode<kTf32>::kN;  // two A buffers and one D per warpgroup
+template <bool kTf32>
+constexpr size_t kRingBytes = (size_t)kXStages * kXBytes + (size_t)kBStages * Mode<kTf32>::kBBytes;
+template <bool kTf32>
+constexpr size_t kSmemBytes = kRingBytes<kTf32> + 1024 + 1024;
 
-static_assert(kWG * kWGCols <= kTmemCols, "TMEM budget");
+static_assert(kWG * kWGCols<false> <= kTmemCols && kWG * kWGCols<true> <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Bookkeeping) <= 1024, "bookkeeping area");
 static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of one slice");
-static_assert(kSmemBytes <= 232448, "dynamic shared memory");
-static_assert(kBBytes % 1024 == 0 && kLimbRowOffset + kLimbRows <= kBRows, "B buffer layout");
+static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynamic shared memory");
+static_assert(Mode<false>::kBBytes % 1024 == 0 && Mode<true>::kBBytes % 1024 == 0 &&
+                  kLimbRowOffset + kLimbRows <= kBRows, "B buffer layout");
 
 // ---------------------------------------------------------------- W limbs
 
@@ -144,6 +174,28 @@ hcmix_pack_limbs_kernel(const float* __restrict__ W, int64_t w_stride, int K,
   for (int p = 0; p < 4; ++p)
     *reinterpret_cast<uint2*>(limbs + ((int64_t)p * kMix + j) * K + k) =
         make_uint2(out[p][0], out[p][1]);
+}
+
+// W[24, K] fp32 -> parts[2][24][K] fp32 for the tf32x3 mode: part 0 is
+// big = W rounded to tf32 (nearest, ties away from zero), part 1 is
+// small = W - big, exact in fp32 and passed to the MMAs as it is (the page
+// hands the unrounded difference to its tf32 dot).  One float4 per thread.
+__global__ void __launch_bounds__(kPackThreads)
+hcmix_pack_tf32_kernel(const float* __restrict__ W, int64_t w_stride, int K,
+                       float* __restrict__ parts) {
+  sm100::grid_launch_dependents();  // the contraction may start streaming x now
+  const int64_t per_row = K / 4;
+  const int64_t i = (int64_t)blockIdx.x * kPackThreads + threadIdx.x;
+  if (i >= kMix * per_row) return;
+  const int j = (int)(i / per_row);
+  const int64_t k = (i % per_row) * 4;
+  const float4 v = *reinterpret_cast<const float4*>(W + (int64_t)j * w_stride + k);
+  const float4 big = make_float4(sm100::cvt_rna_tf32(v.x), sm100::cvt_rna_tf32(v.y),
+                                 sm100::cvt_rna_tf32(v.z), sm100::cvt_rna_tf32(v.w));
+  const float4 small = make_float4(__fsub_rn(v.x, big.x), __fsub_rn(v.y, big.y),
+                                   __fsub_rn(v.z, big.z), __fsub_rn(v.w, big.w));
+  *reinterpret_cast<float4*>(parts + (int64_t)j * K + k) = big;
+  *reinterpret_cast<float4*>(parts + (int64_t)(kMix + j) * K + k) = small;
 }
 
 // ---------------------------------------------------------------- main kernel
@@ -201,6 +253,7 @@ __device__ __forceinline__ void fail(Bookkeeping& bk, uint32_t* err) {
   *reinterpret_cast<volatile int*>(&bk.abort) = 1;
 }
 
+template <bool kTf32>
 __global__ void __launch_bounds__(kThreads, 1)
 hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, int n_tiles, int Mpad,
@@ -209,7 +262,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Bookkeeping& bk = *reinterpret_cast<Bookkeeping*>(smem + kRingBytes);
+  using MD = Mode<kTf32>;
+  constexpr uint32_t kWGC = kWGCols<kTf32>;
+  Bookkeeping& bk = *reinterpret_cast<Bookkeeping*>(smem + kRingBytes<kTf32>);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int64_t G = gridDim.x, b = blockIdx.x;
@@ -217,7 +272,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const int n = (int)((b + 1) * n_units / G - u_begin);
 
   auto x_smem = [&](int st) { return smem + (size_t)st * kXBytes; };
-  auto b_smem = [&](int st) { return smem + (size_t)kXStages * kXBytes + (size_t)st * kBBytes; };
+  auto b_smem = [&](int st) { return smem + (size_t)kXStages * kXBytes + (size_t)st * MD::kBBytes; };
 
   // ---- set-up: barriers, the zero rows of every B buffer, TMEM
   if (threadIdx.x == 0) {
@@ -238,8 +293,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     bk.never = 0;
     fence_mbarrier_init();
   }
-  {
-    // rows 0..23 of each B buffer stay zero (the limbs are loaded to rows 24..119)
+  if constexpr (!kTf32) {
+    // rows 0..23 of each B buffer stay zero (the limbs are loaded to rows 24..119;
+    // the tf32x3 boxes bring their own zero rows)
     constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
     for (int idx = threadIdx.x; idx < kBStages * kUnits; idx += kThreads) {
       const int s = idx / kUnits, u = idx % kUnits;
@@ -324,9 +380,13 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
               break;
             }
             const uint32_t full = smem_u32(&bk.full_b[j]);
-            mbar_arrive_expect_tx(full, kBTxBytes);
-            tma_load_2d(smem_u32(b_smem(j)) + kLimbRowOffset * kRowBytes, &tmap_w,
-                        (sl * kChunksPerSlice + c) * kChunk, 0, full, pol);
+            mbar_arrive_expect_tx(full, MD::kBTxBytes);
+            if constexpr (kTf32)  // both parts, both 32-column halves of the chunk
+              tma_load_4d(smem_u32(b_smem(j)), &tmap_w, 0, 0,
+                          2 * (sl * kChunksPerSlice + c), 0, full, pol);
+            else
+              tma_load_2d(smem_u32(b_smem(j)) + kLimbRowOffset * kRowBytes, &tmap_w,
+                          (sl * kChunksPerSlice + c) * kChunk, 0, full, pol);
           }
           ++loads[g];
         }
@@ -394,16 +454,32 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                          abort_flag, kWaitLimitNs)));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a = tmem + (uint32_t)g * kWGCols + aph * kACols;
-          const uint32_t d = tmem + (uint32_t)g * kWGCols + 2 * kACols;
+          const uint32_t a = tmem + (uint32_t)g * kWGC + aph * kACols;
+          const uint32_t d = tmem + (uint32_t)g * kWGC + 2 * kACols;
           const uint32_t bb = smem_u32(b_smem(j));
+          if constexpr (kTf32) {
+            // K-step q covers columns 8q..8q+7: half q / 4 of the part, 32 bytes
+            // per step inside its 128-byte rows
+            constexpr uint32_t kHalf = kTf32Rows * kRowBytes, kPart = 2 * kHalf;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)  // x1 against [0 | w0 | w1 | w2]
-            umma_bf16_ts_warp(d, a + 32 + 8 * q, smem_desc_sw128(bb + 32 * q), kIdesc, q > 0);
+            for (int q = 0; q < 8; ++q)  // dot(x, small), from zero
+              umma_tf32_ts_warp(d, a + 8 * q,
+                                smem_desc_sw128(bb + kPart + (q >> 2) * kHalf + 32 * (q & 3)),
+                                MD::kIdesc, q > 0);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)  // x0 against [w0 | w1 | w2 | w3]
-            umma_bf16_ts_warp(d, a + 8 * q,
-                              smem_desc_sw128(bb + kLimbRowOffset * kRowBytes + 32 * q), kIdesc, 1);
+            for (int q = 0; q < 8; ++q)  // + dot(x, big)
+              umma_tf32_ts_warp(d, a + 8 * q,
+                                smem_desc_sw128(bb + (q >> 2) * kHalf + 32 * (q & 3)), MD::kIdesc, 1);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)  // x1 against [0 | w0 | w1 | w2]
+              umma_bf16_ts_warp(d, a + 32 + 8 * q, smem_desc_sw128(bb + 32 * q), MD::kIdesc, q > 0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)  // x0 against [w0 | w1 | w2 | w3]
+              umma_bf16_ts_warp(d, a + 8 * q,
+                                smem_desc_sw128(bb + kLimbRowOffset * kRowBytes + 32 * q),
+                                MD::kIdesc, 1);
+          }
           umma_commit_warp(smem_u32(&bk.d_ready[g]));
           if (last_use[g]) umma_commit_warp(smem_u32(&bk.empty_b[j]));
         }
@@ -418,7 +494,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t a_base = tmem + (uint32_t)g * kWGCols;
+    const uint32_t a_base = tmem + (uint32_t)g * kWGC;
     const uint32_t d_col = a_base + 2 * kACols;
     // byte offsets of the row's 16-byte pieces p in a swizzled x tile
     uint32_t xoff[8];
@@ -448,12 +524,24 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         xw[4 * p] = v.x; xw[4 * p + 1] = v.y; xw[4 * p + 2] = v.z; xw[4 * p + 3] = v.w;
       }
       tsq = sq_tree64_f32x2(xw);
-      // x0 = x rounded to the grid 2^(ex-5) with the bf16 magic constant
-      // 1.5 * 2^(ex+2) (x + magic stays in one binade, so one bf16 rounding
-      // puts x on the grid); x1 = x - x0 is exact.  Both are bf16, <= 8 bits.
-      const uint32_t magic = bf16x2_split_magic(xw);
       const uint32_t a_col = a_base + (uint32_t)(k & 1) * kACols;
-      {
+      if constexpr (kTf32) {
+        // x as fp32 (bf16 is exact in tf32), column c = chunk column c
+        uint32_t lo[32], hi[32];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          lo[2 * t] = xw[t] << 16;
+          lo[2 * t + 1] = xw[t] & 0xffff0000u;
+          hi[2 * t] = xw[16 + t] << 16;
+          hi[2 * t + 1] = xw[16 + t] & 0xffff0000u;
+        }
+        tmem_st32(lanes | a_col, lo);
+        tmem_st32(lanes | (a_col + 32), hi);
+      } else {
+        // x0 = x rounded to the grid 2^(ex-5) with the bf16 magic constant
+        // 1.5 * 2^(ex+2) (x + magic stays in one binade, so one bf16 rounding
+        // puts x on the grid); x1 = x - x0 is exact.  Both are bf16, <= 8 bits.
+        const uint32_t magic = bf16x2_split_magic(xw);
         uint32_t w0[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
@@ -492,12 +580,18 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // D = [top | r1 | r2 | r3]; chunk dot = top + ((r1 + r2) + r3), in output
-      // pairs; all 96 columns in one TMEM round trip
-      uint32_t dv[4 * kMix];
-      tmem_ld32(lanes | d_col, dv);
-      tmem_ld32(lanes | (d_col + 32), dv + 32);
-      tmem_ld32(lanes | (d_col + 64), dv + 64);
+      // exact: D = [top | r1 | r2 | r3]; chunk dot = top + ((r1 + r2) + r3), in
+      // output pairs; all 96 columns in one TMEM round trip.  tf32x3: D's first
+      // 24 columns are the chunk dot.
+      uint32_t dv[kTf32 ? kMix : 4 * kMix];
+      if constexpr (kTf32) {
+        tmem_ld16(lanes | d_col, dv);
+        tmem_ld8(lanes | (d_col + 16), dv + 16);
+      } else {
+        tmem_ld32(lanes | d_col, dv);
+        tmem_ld32(lanes | (d_col + 32), dv + 32);
+        tmem_ld32(lanes | (d_col + 64), dv + 64);
+      }
       tmem_wait_ld();
       // A(k+1) is written and D has been read: the MMAs of chunk k+1 may run
       // while this chunk's dot is formed
@@ -510,10 +604,14 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
 #pragma unroll
       for (int j = 0; j < kMix / 2; ++j) {
         const float2 top = make_float2(__uint_as_float(dv[2 * j]), __uint_as_float(dv[2 * j + 1]));
-        const float2 u = make_float2(__uint_as_float(dv[kMix + 2 * j]), __uint_as_float(dv[kMix + 2 * j + 1]));
-        const float2 v = make_float2(__uint_as_float(dv[2 * kMix + 2 * j]), __uint_as_float(dv[2 * kMix + 2 * j + 1]));
-        const float2 w = make_float2(__uint_as_float(dv[3 * kMix + 2 * j]), __uint_as_float(dv[3 * kMix + 2 * j + 1]));
-        acc[j] = __fadd2_rn(acc[j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
+        if constexpr (kTf32) {
+          acc[j] = __fadd2_rn(acc[j], top);
+        } else {
+          const float2 u = make_float2(__uint_as_float(dv[kMix + 2 * j]), __uint_as_float(dv[kMix + 2 * j + 1]));
+          const float2 v = make_float2(__uint_as_float(dv[2 * kMix + 2 * j]), __uint_as_float(dv[2 * kMix + 2 * j + 1]));
+          const float2 w = make_float2(__uint_as_float(dv[3 * kMix + 2 * j]), __uint_as_float(dv[3 * kMix + 2 * j + 1]));
+          acc[j] = __fadd2_rn(acc[j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
+        }
       }
       sqs = __fadd_rn(sqs, tsq_cur);
       tsq_cur = tsq_next;
@@ -602,51 +700,87 @@ inline bool make_map_bf16_3d_chunks(CUtensorMap* map, const void* base, uint64_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace tc
+// 4-D view of the tf32x3 parts[2][24][K] (fp32) as [part][K / 32 halves]
+// [24 rows][32]: one box is both parts of two consecutive 32-column halves
+// (one chunk) with 32 rows, stored in shared memory as [part][half][32 rows x
+// 128 B] with the 128-byte swizzle; rows 24..31 lie past the tensor and are
+// filled with zeros.
+inline bool make_map_tf32_parts(CUtensorMap* map, const float* parts, uint64_t K) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {32, (cuuint64_t)kMix, K / 32, 2};
+  const cuuint64_t strides[3] = {K * 4, 128, (cuuint64_t)kMix * K * 4};
+  const cuuint32_t box[4] = {32, kTf32Rows, 2, 2};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(parts), dims, strides,
+            box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
-// Packs W into limbs, then runs the tensor-core contraction into `part`.
-inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* W,
-                              int64_t w_stride, int64_t M, int64_t K, uint16_t* limbs,
-                              float* part, int Mpad, uint32_t* err, cudaStream_t stream) {
-  const int nch = (int)(K / kChunk);
-  const int pack_blocks = (kMix * nch + tc::kPackTasksPerBlock - 1) / tc::kPackTasksPerBlock;
-  tc::hcmix_pack_limbs_kernel<<<pack_blocks, tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K,
-                                                                           limbs);
-  if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
-
-  CUtensorMap mx, mw;
-  if (!tc::make_map_bf16_3d_chunks(&mx, x, (uint64_t)K, (uint64_t)M, (uint64_t)x_stride * 2,
-                                    tc::kTileM, tc::kChunksPerStage) ||
-      !tc::make_map_bf16_2d(&mw, limbs, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
-                            tc::kLimbRows))
-    return HCMIX_ERR_CUDA;
-
+template <bool kTf32>
+hcmix_status launch_main(const CUtensorMap& mx, const CUtensorMap& mw, int64_t M, int64_t K,
+                         float* part, int Mpad, uint32_t* err, cudaStream_t stream) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return HCMIX_ERR_CUDA;
-  const int64_t n_tiles = (M + tc::kTileM - 1) / tc::kTileM;
+  const int64_t n_tiles = (M + kTileM - 1) / kTileM;
   const int64_t n_units = n_tiles * (K / kSlice);
   const int64_t grid = n_units < sms ? n_units : sms;
-  if (cudaFuncSetAttribute(tc::hcmix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tc::kSmemBytes) != cudaSuccess)
+  if (cudaFuncSetAttribute(hcmix_tc_kernel<kTf32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes<kTf32>) != cudaSuccess)
     return HCMIX_ERR_CUDA;
   // launched as a programmatic dependent of the pack kernel: x streams while
-  // the limbs are being written; the W producer waits for them
+  // W is being packed; the W producer waits for the pack grid
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(tc::kThreads);
-  cfg.dynamicSmemBytes = tc::kSmemBytes;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes<kTf32>;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tc::hcmix_tc_kernel, mx, mw, (int)n_tiles, Mpad, n_units, part,
+  if (cudaLaunchKernelEx(&cfg, hcmix_tc_kernel<kTf32>, mx, mw, (int)n_tiles, Mpad, n_units, part,
                          err) != cudaSuccess)
     return HCMIX_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
+}
+
+}  // namespace tc
+
+// Packs W (exact limbs, or the tf32x3 big / small parts), then runs the
+// tensor-core contraction into `part`.  `packed` is the workspace area of
+// 4 * 24 * K * 2 bytes (= 2 * 24 * K * 4) that holds the packed W.
+inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* W,
+                              int64_t w_stride, int64_t M, int64_t K, void* packed,
+                              float* part, int Mpad, uint32_t* err, cudaStream_t stream,
+                              bool tf32x3) {
+  CUtensorMap mx, mw;
+  if (!tc::make_map_bf16_3d_chunks(&mx, x, (uint64_t)K, (uint64_t)M, (uint64_t)x_stride * 2,
+                                    tc::kTileM, tc::kChunksPerStage))
+    return HCMIX_ERR_CUDA;
+  if (tf32x3) {
+    float* parts = static_cast<float*>(packed);
+    const int64_t n4 = kMix * (K / 4);
+    tc::hcmix_pack_tf32_kernel<<<(unsigned)((n4 + tc::kPackThreads - 1) / tc::kPackThreads),
+                                 tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K, parts);
+    if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
+    if (!tc::make_map_tf32_parts(&mw, parts, (uint64_t)K)) return HCMIX_ERR_CUDA;
+    return tc::launch_main<true>(mx, mw, M, K, part, Mpad, err, stream);
+  }
+  uint16_t* limbs = static_cast<uint16_t*>(packed);
+  const int nch = (int)(K / kChunk);
+  const int pack_blocks = (kMix * nch + tc::kPackTasksPerBlock - 1) / tc::kPackTasksPerBlock;
+  tc::hcmix_pack_limbs_kernel<<<pack_blocks, tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K,
+                                                                           limbs);
+  if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
+  if (!tc::make_map_bf16_2d(&mw, limbs, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
+                            tc::kLimbRows))
+    return HCMIX_ERR_CUDA;
+  return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, stream);
 }
 
 }  // namespace hcmix

@@ -68,12 +68,25 @@ typedef enum {
  * totals stored in the workspace, then an ordered reduce) against the page's
  * fused kernel (one CTA per row block walks all of K and keeps the running
  * total, so only the total is stored; the page's module docstring).  Their
- * statistics are bit-identical. */
+ * statistics are bit-identical.
+ *
+ * HCMIX_PATH_TC_TF32X3 is the page's own chunk arithmetic (hc_fused page,
+ * module docstring, second bullet; _tf32_rna and the two tl.dot calls of
+ * _hc_mix_fullk_kernel) on the tensor-core kernel: W = big + small with
+ * big = W rounded to tf32 (nearest, ties away) and small = W - big; every
+ * chunk dot is dot(x, small) from zero followed by dot(x, big) on top, as
+ * tcgen05 kind::tf32 MMAs.  The tensor core's internal rounding sets the last
+ * bits of each chunk dot, so this path is NOT held to the mix tolerance above.
+ * Per chunk its error is at most (2^-19 + 2^-21) * sum |x| |W| over the chunk
+ * (16 fp32 accumulations and the tf32 truncation of the small part), and its
+ * tests hold each output within 2^-18 * sum_k |x[m,k]| |W[j,k]| of the exact
+ * result; sq is bit-identical to the other paths.  AUTO never selects it. */
 typedef enum {
   HCMIX_PATH_AUTO = 0,
   HCMIX_PATH_SIMT = 1,       /* CUDA-core split-K kernel (stock layout) */
   HCMIX_PATH_TC = 2,         /* tcgen05 tensor-core split-K kernel */
-  HCMIX_PATH_SIMT_FULLK = 3  /* CUDA-core full-K kernel (the page's fused design) */
+  HCMIX_PATH_SIMT_FULLK = 3, /* CUDA-core full-K kernel (the page's fused design) */
+  HCMIX_PATH_TC_TF32X3 = 4   /* tensor-core split-K kernel with the page's tf32x3 chunk dots */
 } hcmix_path;
 
 /* Bytes of device workspace that hc_mix_stats / hc_mix_fused need for M rows.

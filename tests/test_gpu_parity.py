@@ -237,6 +237,75 @@ def test_fullk_bit_identical_to_split_k(M, K):
         assert np.array_equal(u.view(np.uint32), v.view(np.uint32)), f"{name} differs"
 
 
+# ---- tf32x3 mode: the page's chunk arithmetic (big = tf32 RNA of W, small =
+# W - big, dot(x, small) then dot(x, big) per chunk as tf32 MMAs).  The tensor
+# core rounds inside every chunk dot, so the mode is held to a bound derived
+# from that arithmetic rather than to the exact path's tolerance: per chunk,
+# 16 accumulations at fp32 precision (16 * 2^-23) plus the tf32 truncation of
+# the small part (2^-21) stay below 2^-19 + 2^-21 of sum |x| |W|, and 2^-18
+# leaves room for the slice and total additions that follow.
+
+def tf32x3_bound(x, W):
+    xf = hi.bf16_bits_to_f32(x).astype(np.float64)
+    return 2.0 ** -18 * (np.abs(xf) @ np.abs(W.astype(np.float64)).T)
+
+
+@pytest.fixture(scope="module")
+def tf32x3():
+    if not path_available("tc_tf32x3"):
+        pytest.fail("kernel path tc_tf32x3 is not available in this library")
+    return "tc_tf32x3"
+
+
+@pytest.mark.parametrize("case", ["m7_k256", "ragged300_k2048", "m16", "m512_outliers", "m4096"])
+def test_tf32x3_within_bound(tf32x3, case):
+    M, K, outl = {"m7_k256": (7, 256, False), "ragged300_k2048": (300, 2048, False),
+                  "m16": (16, 20480, False), "m512_outliers": (512, 20480, True),
+                  "m4096": (4096, 20480, False)}[case]
+    x, W = hi.make_x(M, K=K, outliers=outl), hi.make_w(K=K)
+    sc, bs = hi.make_scale(), hi.make_base()
+    want_mix, want_sq = oracle.stats(x, W, threads=THREADS)
+    got = run(x, W, sc, bs, tf32x3)
+    d = np.abs(got[3].astype(np.float64) - want_mix)
+    bound = tf32x3_bound(x, W)
+    assert (d <= bound).all(), f"{case}: {(d > bound).sum()} outputs beyond 2^-18 sum|x||W|"
+    assert np.array_equal(got[4], want_sq), f"{case}: sq not bit-identical"
+    # the epilogue of this path's own statistics
+    want_ep = oracle.epilogue(got[3], got[4], K, sc, bs, threads=THREADS)
+    assert_epilogue_close(got[:3], want_ep, case)
+    print(f"tf32x3 {case}: max |mix error| / bound = {(d / bound).max():.4f}")
+
+
+def test_tf32x3_exact_on_grid_inputs(tf32x3):
+    """x in {-2..2}, W = a + b 2^-12 with a, b in {-5..5}: W splits into a big
+    part and a small part that tf32 holds exactly, every product and every
+    partial sum the MMAs, the slices and the total form is a multiple of
+    2^-12 below 2^10, so the result is the exact sum.  A dropped small part,
+    a wrong sign, column or chunk shows up as a wrong bit pattern."""
+    rng = np.random.default_rng(11)
+    M, K = 130, 1024
+    xi = rng.integers(-2, 3, size=(M, K)).astype(np.float64)
+    W64 = rng.integers(-5, 6, size=(24, K)) + rng.integers(-5, 6, size=(24, K)) * 2.0 ** -12
+    W = W64.astype(np.float32)
+    assert np.array_equal(W.astype(np.float64), W64)
+    # every partial sum the path forms stays below 2^10 on the 2^-12 grid
+    prods = xi[:, None, :] * W64[None, :, :]
+    chunk = prods.reshape(M, 24, K // 64, 64)
+    assert (np.abs(chunk).sum(axis=3) < 2 ** 10).all()
+    cd = chunk.sum(axis=3)  # chunk dots, exact
+    slices = cd.reshape(M, 24, K // 256, 4)
+    assert (np.abs(np.cumsum(slices, axis=3)) < 2 ** 10).all()
+    assert (np.abs(np.cumsum(slices.sum(axis=3), axis=2)) < 2 ** 10).all()
+    exact = prods.sum(axis=2)
+    got = run(hi.bf16_bits_from_f64(xi), W, hi.make_scale(), hi.make_base(), tf32x3)
+    assert np.array_equal(got[3].astype(np.float64), exact), "tf32x3 grid inputs not exact"
+
+
+def test_tf32x3_is_not_auto():
+    assert binding.hc_mix_auto_path(4096) != "tc_tf32x3"
+    assert binding.hc_mix_auto_path(1) != "tc_tf32x3"
+
+
 def test_stack86_m16384_sampled():
     """The 43-layer stack: 86 calls at M=16384 with distinct W / scale / base,
     captured once in a CUDA graph as the benchmark runs it.  Sampled rows of every
