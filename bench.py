@@ -469,7 +469,8 @@ def run_sweep(args):
     # stock split-K -> fused full-K, us per call), here on the same CUDA-core
     # arithmetic, with the tensor-core split-K path beside them.
     designs = {"simt": "stock split-K (CUDA cores)", "simt_fullk": "fused full-K (CUDA cores)",
-               "tc": "split-K (tensor cores)"}
+               "tc": "split-K (tensor cores)",
+               "tc_tf32x3": "split-K (tensor cores, the page's tf32x3 chunk dots)"}
     x4096 = hi.make_x(4096)
     for M in (512, 1024, 2048, 4096):
         x = torch.from_numpy(np.ascontiguousarray(x4096[:M]).view(np.int16)).view(
