@@ -219,7 +219,8 @@ hcmix_status hc_mix_sinkhorn(const float* mix, const float* sq, int64_t M, int64
   if (M == 0) return HCMIX_OK;
   if (mix == nullptr || sq == nullptr) return HCMIX_ERR_INVALID_ARG;
   const float inv_k = (float)(1.0 / (double)K);
-  hcmix_epilogue_kernel<<<(unsigned)((M + 127) / 128), 128, 0, static_cast<cudaStream_t>(stream)>>>(
+  hcmix_epilogue_kernel<<<(unsigned)((M + kReduceRows - 1) / kReduceRows), kEpilogueThreads, 0,
+                          static_cast<cudaStream_t>(stream)>>>(
       mix, sq, (int)M, inv_k, hc_scale, hc_base, sinkhorn_iters, rms_eps, hc_eps, pre, post, comb);
   return launch_status();
 }

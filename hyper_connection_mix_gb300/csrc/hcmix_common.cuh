@@ -98,52 +98,4 @@ __device__ __forceinline__ float sq_tree64(const uint32_t (&w)[32]) {
   return __fadd_rn(v[0], v[32]);
 }
 
-// Epilogue for one row (task statement's formulae; every operation one IEEE
-// round-to-nearest fp32 operation, Sinkhorn sums in index order).
-__device__ __forceinline__ void epilogue_row(const float (&mixv)[kMix], float sq, float inv_k,
-                                             const float* __restrict__ hc_scale,
-                                             const float* __restrict__ hc_base, int iters,
-                                             float rms_eps, float hc_eps, float* __restrict__ pre,
-                                             float* __restrict__ post, float* __restrict__ comb) {
-  const float v = __fadd_rn(__fmul_rn(sq, inv_k), rms_eps);
-  const float r = __fdiv_rn(1.0f, __fsqrt_rn(v));
-  const float s0 = hc_scale[0], s1 = hc_scale[1], s2 = hc_scale[2];
-  float lg[kMix];
-#pragma unroll
-  for (int j = 0; j < kMix; ++j) {
-    const float sc = j < kHc ? s0 : (j < 2 * kHc ? s1 : s2);
-    lg[j] = __fadd_rn(__fmul_rn(__fmul_rn(mixv[j], r), sc), hc_base[j]);
-  }
-#pragma unroll
-  for (int i = 0; i < kHc; ++i) {
-    pre[i] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lg[i])));
-    post[i] = __fmul_rn(2.0f, __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lg[kHc + i]))));
-  }
-  float c[kHc * kHc];
-#pragma unroll
-  for (int e = 0; e < kHc * kHc; ++e) c[e] = expf(lg[2 * kHc + e]);
-  for (int it = 0; it < iters; ++it) {
-#pragma unroll
-    for (int i = 0; i < kHc; ++i) {
-      float s = c[i * kHc];
-#pragma unroll
-      for (int j = 1; j < kHc; ++j) s = __fadd_rn(s, c[i * kHc + j]);
-      const float den = __fadd_rn(s, hc_eps);
-#pragma unroll
-      for (int j = 0; j < kHc; ++j) c[i * kHc + j] = __fdiv_rn(c[i * kHc + j], den);
-    }
-#pragma unroll
-    for (int j = 0; j < kHc; ++j) {
-      float s = c[j];
-#pragma unroll
-      for (int i = 1; i < kHc; ++i) s = __fadd_rn(s, c[i * kHc + j]);
-      const float den = __fadd_rn(s, hc_eps);
-#pragma unroll
-      for (int i = 0; i < kHc; ++i) c[i * kHc + j] = __fdiv_rn(c[i * kHc + j], den);
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < kHc * kHc; ++e) comb[e] = c[e];
-}
-
 }  // namespace hcmix

@@ -8,8 +8,8 @@
 // Layout: 32 rows per CTA and one warp per output j (25 warps, one row per
 // lane), so every load of a (slice, j) pair is 32 consecutive floats.  Each
 // lane issues its slice loads in batches of 40 before adding them in slice
-// order, so the L2 latency is paid per batch rather than per slice.  Warp 0
-// then runs the epilogue, one row per lane.
+// order, so the L2 latency is paid per batch rather than per slice.  The
+// first 512 threads then run the epilogue, 16 per row.
 #pragma once
 
 #include "hcmix_common.cuh"
@@ -20,43 +20,19 @@ constexpr int kReduceRows = 32;
 constexpr int kReduceThreads = 32 * kPartStride;
 constexpr int kReduceBatch = 40;
 
-__global__ void __launch_bounds__(kReduceThreads)
-hcmix_reduce_kernel(const float* __restrict__ part, int n_slices, int Mpad, int M, float inv_k,
-                    const float* __restrict__ hc_scale, const float* __restrict__ hc_base,
-                    int iters, float rms_eps, float hc_eps, float* __restrict__ pre,
-                    float* __restrict__ post, float* __restrict__ comb,
-                    float* __restrict__ mix_out, float* __restrict__ sq_out, int do_epilogue) {
-  __shared__ float s_tot[kPartStride][kReduceRows + 1];
-  const int lane = threadIdx.x & 31, out = threadIdx.x >> 5;  // out: mix index or 24 (sq)
-  const int lrow = blockIdx.x * kReduceRows + lane;
-  float t = 0.0f;
-  if (lrow < M) {
-    const float* p = part + (int64_t)out * Mpad + lrow;
-    const int64_t step = (int64_t)kPartStride * Mpad;
-    int s = 0;
-    for (; s + kReduceBatch <= n_slices; s += kReduceBatch) {
-      float v[kReduceBatch];
-#pragma unroll
-      for (int q = 0; q < kReduceBatch; ++q) v[q] = __ldg(p + (int64_t)(s + q) * step);
-#pragma unroll
-      for (int q = 0; q < kReduceBatch; ++q) t = __fadd_rn(t, v[q]);
-    }
-    for (; s < n_slices; ++s) t = __fadd_rn(t, __ldg(p + (int64_t)s * step));
-  }
-  s_tot[out][lane] = t;
-  __syncthreads();
+// Epilogue of the CTA's 32 rows from their totals in shared memory
+// (s_tot[j][r]: j < 24 mix, j = 24 sum of squares): 16 threads per row,
+// thread e owns comb entry e = 4i + j and, for e < 8, logit e of pre (e < 4)
+// or post.  Sinkhorn sums are gathered with shuffles and added in index
+// order, as one thread per row would.  Threads 512 and up do nothing.
+__device__ __forceinline__ void epilogue16(const float (&s_tot)[kPartStride][kReduceRows + 1],
+                                           int row0, int M, float inv_k,
+                                           const float* __restrict__ hc_scale,
+                                           const float* __restrict__ hc_base, int iters,
+                                           float rms_eps, float hc_eps, float* __restrict__ pre,
+                                           float* __restrict__ post, float* __restrict__ comb) {
   const int tid = threadIdx.x;
-  const int row0 = blockIdx.x * kReduceRows;
-  if (mix_out != nullptr && tid < kReduceRows * kMix) {
-    const int r = tid / kMix, jj = tid % kMix;
-    if (row0 + r < M) mix_out[(int64_t)(row0 + r) * kMix + jj] = s_tot[jj][r];
-  }
-  if (sq_out != nullptr && tid < kReduceRows && row0 + tid < M) sq_out[row0 + tid] = s_tot[kMix][tid];
-  if (!do_epilogue || tid >= kReduceRows * kHc * kHc) return;
-
-  // Epilogue: 16 threads per row, thread e owns comb entry e = 4i + j and, for
-  // e < 8, logit e of pre (e < 4) or post.  Sinkhorn sums are gathered with
-  // shuffles and added in index order, as one thread per row would.
+  if (tid >= kReduceRows * kHc * kHc) return;
   const int rloc = tid >> 4, e = tid & 15;
   const int row = row0 + rloc;
   const int gbase = threadIdx.x & 16;  // first lane of this row's 16-lane group
@@ -91,21 +67,64 @@ hcmix_reduce_kernel(const float* __restrict__ part, int n_slices, int Mpad, int 
   if (row < M) comb[(int64_t)row * kHc * kHc + e] = c;
 }
 
-// The epilogue alone from caller-provided mix[M, 24] and sq[M].
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kReduceThreads)
+hcmix_reduce_kernel(const float* __restrict__ part, int n_slices, int Mpad, int M, float inv_k,
+                    const float* __restrict__ hc_scale, const float* __restrict__ hc_base,
+                    int iters, float rms_eps, float hc_eps, float* __restrict__ pre,
+                    float* __restrict__ post, float* __restrict__ comb,
+                    float* __restrict__ mix_out, float* __restrict__ sq_out, int do_epilogue) {
+  __shared__ float s_tot[kPartStride][kReduceRows + 1];
+  const int lane = threadIdx.x & 31, out = threadIdx.x >> 5;  // out: mix index or 24 (sq)
+  const int lrow = blockIdx.x * kReduceRows + lane;
+  float t = 0.0f;
+  if (lrow < M) {
+    const float* p = part + (int64_t)out * Mpad + lrow;
+    const int64_t step = (int64_t)kPartStride * Mpad;
+    int s = 0;
+    for (; s + kReduceBatch <= n_slices; s += kReduceBatch) {
+      float v[kReduceBatch];
+#pragma unroll
+      for (int q = 0; q < kReduceBatch; ++q) v[q] = __ldg(p + (int64_t)(s + q) * step);
+#pragma unroll
+      for (int q = 0; q < kReduceBatch; ++q) t = __fadd_rn(t, v[q]);
+    }
+    for (; s < n_slices; ++s) t = __fadd_rn(t, __ldg(p + (int64_t)s * step));
+  }
+  s_tot[out][lane] = t;
+  __syncthreads();
+  const int tid = threadIdx.x;
+  const int row0 = blockIdx.x * kReduceRows;
+  if (mix_out != nullptr && tid < kReduceRows * kMix) {
+    const int r = tid / kMix, jj = tid % kMix;
+    if (row0 + r < M) mix_out[(int64_t)(row0 + r) * kMix + jj] = s_tot[jj][r];
+  }
+  if (sq_out != nullptr && tid < kReduceRows && row0 + tid < M) sq_out[row0 + tid] = s_tot[kMix][tid];
+  if (!do_epilogue) return;
+  epilogue16(s_tot, row0, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post, comb);
+}
+
+// The epilogue alone from caller-provided mix[M, 24] and sq[M]: 32 rows per
+// CTA staged in shared memory in the reduce kernel's layout, then the same
+// 16-threads-per-row epilogue.
+constexpr int kEpilogueThreads = kReduceRows * kHc * kHc;
+
+__global__ void __launch_bounds__(kEpilogueThreads)
 hcmix_epilogue_kernel(const float* __restrict__ mix, const float* __restrict__ sq, int M,
                       float inv_k, const float* __restrict__ hc_scale,
                       const float* __restrict__ hc_base, int iters, float rms_eps, float hc_eps,
                       float* __restrict__ pre, float* __restrict__ post,
                       float* __restrict__ comb) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= M) return;
-  float mixv[kMix];
-#pragma unroll
-  for (int j = 0; j < kMix; ++j) mixv[j] = mix[(int64_t)row * kMix + j];
-  epilogue_row(mixv, sq[row], inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps,
-               pre + (int64_t)row * kHc, post + (int64_t)row * kHc,
-               comb + (int64_t)row * kHc * kHc);
+  __shared__ float s_tot[kPartStride][kReduceRows + 1];
+  const int row0 = blockIdx.x * kReduceRows;
+  const int rows = min(kReduceRows, M - row0);
+  for (int i = threadIdx.x; i < kReduceRows * kMix; i += kEpilogueThreads) {
+    const int r = i / kMix, j = i % kMix;
+    s_tot[j][r] = r < rows ? mix[(int64_t)(row0 + r) * kMix + j] : 0.0f;
+  }
+  if (threadIdx.x < kReduceRows)
+    s_tot[kMix][threadIdx.x] = (int)threadIdx.x < rows ? sq[row0 + threadIdx.x] : 0.0f;
+  __syncthreads();
+  epilogue16(s_tot, row0, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post, comb);
 }
 
 }  // namespace hcmix

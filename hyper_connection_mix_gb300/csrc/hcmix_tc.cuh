@@ -248,6 +248,121 @@ __device__ __forceinline__ float sq_tree64_f32x2(const uint32_t (&w)[32]) {
   return __fadd_rn(h[0], h[1]);                                      // the two halves
 }
 
+// One chunk's MMAs and the commit to `bar` from one asm block: the whole
+// (converged) warp runs it and the lane that elect.sync picks issues every
+// instruction, so the issuer spends a few instructions per MMA.  `a` is the
+// chunk's TMEM A buffer, `bdesc` the descriptor of its B buffer; a K-step
+// advances the B start address by 32 bytes (2 descriptor units).
+//
+// Exact limbs: x1 (A columns 32..63) against B rows 0..95 = [0 | w0 | w1 | w2]
+// from zero, then x0 (A columns 0..31) against rows 24..119 = [w0 | w1 | w2 |
+// w3] (+3072 bytes = 192 units), four K-steps of 16 each.
+__device__ __forceinline__ void mma_chunk_exact(uint32_t d, uint32_t a, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t bar) {
+  asm volatile(
+      "{\n\t"
+      ".reg .pred e, pz, pa;\n\t"
+      ".reg .b32 ta;\n\t"
+      ".reg .b64 tb;\n\t"
+      "setp.ne.b32 pz, %1, %1;\n\t"
+      "setp.eq.b32 pa, %1, %1;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "add.u32 ta, %1, 32;\n\t"
+      "add.u64 tb, %2, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, pz;\n\t"
+      "add.u32 ta, %1, 40;\n\t"
+      "add.u64 tb, %2, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 48;\n\t"
+      "add.u64 tb, %2, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 56;\n\t"
+      "add.u64 tb, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 0;\n\t"
+      "add.u64 tb, %2, 192;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 8;\n\t"
+      "add.u64 tb, %2, 194;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 16;\n\t"
+      "add.u64 tb, %2, 196;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 24;\n\t"
+      "add.u64 tb, %2, 198;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, pa;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}"
+      ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(bar)
+      : "memory");
+}
+
+// tf32x3: dot(x, small) from zero, then + dot(x, big); eight K-steps of 8
+// columns each (A columns 8q..), K-step q in half q / 4 (+4096 bytes = 256
+// units) at 32 bytes per step, the small part 8192 bytes (512 units) after
+// the big one.
+__device__ __forceinline__ void mma_chunk_tf32x3(uint32_t d, uint32_t a, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t bar) {
+  asm volatile(
+      "{\n\t"
+      ".reg .pred e, pz, pa;\n\t"
+      ".reg .b32 ta;\n\t"
+      ".reg .b64 tb;\n\t"
+      "setp.ne.b32 pz, %1, %1;\n\t"
+      "setp.eq.b32 pa, %1, %1;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "add.u32 ta, %1, 0;\n\t"
+      "add.u64 tb, %2, 512;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pz;\n\t"
+      "add.u32 ta, %1, 8;\n\t"
+      "add.u64 tb, %2, 514;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 16;\n\t"
+      "add.u64 tb, %2, 516;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 24;\n\t"
+      "add.u64 tb, %2, 518;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 32;\n\t"
+      "add.u64 tb, %2, 768;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 40;\n\t"
+      "add.u64 tb, %2, 770;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 48;\n\t"
+      "add.u64 tb, %2, 772;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 56;\n\t"
+      "add.u64 tb, %2, 774;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 0;\n\t"
+      "add.u64 tb, %2, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 8;\n\t"
+      "add.u64 tb, %2, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 16;\n\t"
+      "add.u64 tb, %2, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 24;\n\t"
+      "add.u64 tb, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 32;\n\t"
+      "add.u64 tb, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 40;\n\t"
+      "add.u64 tb, %2, 258;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 48;\n\t"
+      "add.u64 tb, %2, 260;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "add.u32 ta, %1, 56;\n\t"
+      "add.u64 tb, %2, 262;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}"
+      ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void fail(Bookkeeping& bk, uint32_t* err) {
   record_device_error(err, kDevWaitTimeout);
   *reinterpret_cast<volatile int*>(&bk.abort) = 1;
@@ -456,31 +571,11 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
           tc_fence_after();
           const uint32_t a = tmem + (uint32_t)g * kWGC + aph * kACols;
           const uint32_t d = tmem + (uint32_t)g * kWGC + 2 * kACols;
-          const uint32_t bb = smem_u32(b_smem(j));
-          if constexpr (kTf32) {
-            // K-step q covers columns 8q..8q+7: half q / 4 of the part, 32 bytes
-            // per step inside its 128-byte rows
-            constexpr uint32_t kHalf = kTf32Rows * kRowBytes, kPart = 2 * kHalf;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)  // dot(x, small), from zero
-              umma_tf32_ts_warp(d, a + 8 * q,
-                                smem_desc_sw128(bb + kPart + (q >> 2) * kHalf + 32 * (q & 3)),
-                                MD::kIdesc, q > 0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)  // + dot(x, big)
-              umma_tf32_ts_warp(d, a + 8 * q,
-                                smem_desc_sw128(bb + (q >> 2) * kHalf + 32 * (q & 3)), MD::kIdesc, 1);
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)  // x1 against [0 | w0 | w1 | w2]
-              umma_bf16_ts_warp(d, a + 32 + 8 * q, smem_desc_sw128(bb + 32 * q), MD::kIdesc, q > 0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)  // x0 against [w0 | w1 | w2 | w3]
-              umma_bf16_ts_warp(d, a + 8 * q,
-                                smem_desc_sw128(bb + kLimbRowOffset * kRowBytes + 32 * q),
-                                MD::kIdesc, 1);
-          }
-          umma_commit_warp(smem_u32(&bk.d_ready[g]));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(b_smem(j)));
+          if constexpr (kTf32)
+            mma_chunk_tf32x3(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_ready[g]));
+          else
+            mma_chunk_exact(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_ready[g]));
           if (last_use[g]) umma_commit_warp(smem_u32(&bk.empty_b[j]));
         }
       }

@@ -18,8 +18,9 @@
  *     column index differs in bit 4, then bit 3, 2, 1, 0, and finally the two
  *     32-column halves (docstring bullet 3; _sq_tree).  Chunk sums feed slice
  *     totals and slice totals feed the grand total exactly like mix.
- *   epilogue (the reduce+Sinkhorn kernel is only named on the page; the
- *     formulae are the benchmark spec's): r = 1/sqrt(sq * (1/K) + rms_eps);
+ *   epilogue (the page names the reduce+Sinkhorn kernel but its text stops
+ *     before that kernel's body, so the formulae are fixed here as the plain
+ *     RMS-scaled logits, sigmoids and Sinkhorn): r = 1/sqrt(sq * (1/K) + rms_eps);
  *     logit[j] = mix[j] * r * hc_scale[g(j)] + hc_base[j] with g = 0 for
  *     j < hc, 1 for hc <= j < 2hc, 2 otherwise; pre = sigmoid(logit[0:hc]);
  *     post = 2 sigmoid(logit[hc:2hc]); comb = sinkhorn_iters rounds of

@@ -1,7 +1,7 @@
 """CUDA path vs the CPU oracle, element by element, through the C ABI.
 
-Tolerances (task statement): mix within max(2e-6 |o|, 1e-6); pre, post and comb
-within 1e-5 absolute.  sq is compared bit for bit: the kernels evaluate the
+Tolerances of the library's parity contract: mix within max(2e-6 |o|, 1e-6);
+pre, post and comb within 1e-5 absolute.  sq is compared bit for bit: the kernels evaluate the
 page's fixed tree on exact squares with the same round-to-nearest adds.
 """
 import os
