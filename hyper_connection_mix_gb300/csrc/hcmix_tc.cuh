@@ -389,7 +389,45 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   auto x_smem = [&](int st) { return smem + (size_t)st * kXBytes; };
   auto b_smem = [&](int st) { return smem + (size_t)kXStages * kXBytes + (size_t)st * MD::kBBytes; };
 
-  // ---- set-up: barriers, the zero rows of every B buffer, TMEM
+  // units are slice-major: unit u is tile u % n_tiles of slice u / n_tiles
+  auto unit_tile = [&](int64_t u) { return (int)(u % n_tiles); };
+  auto unit_slice = [&](int64_t u) { return (int)(u / n_tiles); };
+
+  // x loads in the producer's order (round, chunk pair, warpgroup); load i
+  // fills stage i % kXStages, each stage two chunks of one unit, released by
+  // its warpgroup.  Issues the loads numbered [from, to) and returns how many
+  // loads were issued in total; ok turns false when a wait for a free stage
+  // gives up.  Loads below kXStages need no free stage.
+  auto x_loads = [&](int from, int to, uint64_t pol, const volatile int* abort_flag,
+                     bool& ok) -> int {
+    int i = 0;
+    for (int r = 0; kWG * r < n; ++r) {
+      const int act = min(kWG, n - kWG * r);
+      for (int c = 0; c < kChunksPerSlice; c += kChunksPerStage) {
+        for (int g = 0; g < act; ++g, ++i) {
+          if (i < from) continue;
+          if (i >= to) return i;
+          const int64_t unit = u_begin + kWG * r + g;
+          const int st = i % kXStages;
+          const uint32_t ph = (uint32_t)(i / kXStages) & 1u;
+          if (i >= kXStages &&
+              !mbar_wait(smem_u32(&bk.empty_x[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            return i;
+          }
+          const uint32_t full = smem_u32(&bk.full_x[st]);
+          mbar_arrive_expect_tx(full, kXTxBytes);
+          tma_load_3d(smem_u32(x_smem(st)), &tmap_x, 0, unit_tile(unit) * kTileM,
+                      unit_slice(unit) * kChunksPerSlice + c, full, pol);
+        }
+      }
+    }
+    return i;
+  };
+
+  // ---- set-up: barriers, the zero rows of every B buffer, TMEM.  Thread 0,
+  // which is also the x producer, starts the first x loads as soon as the
+  // barriers exist, so their DRAM latency overlaps the rest of the set-up.
   if (threadIdx.x == 0) {
     for (int s = 0; s < kXStages; ++s) {
       mbar_init(smem_u32(&bk.full_x[s]), 1);
@@ -407,6 +445,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     bk.abort = 0;
     bk.never = 0;
     fence_mbarrier_init();
+    prefetch_tensormap(&tmap_x);
+    bool ok = true;
+    x_loads(0, kXStages, l2_policy_evict_first(), &bk.never, ok);
   }
   if constexpr (!kTf32) {
     // rows 0..23 of each B buffer stay zero (the limbs are loaded to rows 24..119;
@@ -429,38 +470,13 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const volatile int* abort_flag = &bk.abort;
   const volatile int* never = &bk.never;
 
-  // units are slice-major: unit u is tile u % n_tiles of slice u / n_tiles
-  auto unit_tile = [&](int64_t u) { return (int)(u % n_tiles); };
-  auto unit_slice = [&](int64_t u) { return (int)(u / n_tiles); };
-
   if (warp == 0) {
-    // ---------------- x producer: stage i holds two chunks of one unit, in
-    // the order (round, chunk pair, warpgroup); released by the warpgroup
+    // ---------------- x producer (thread 0): the loads after the first
+    // kXStages, each once its stage has been released
     if (lane == 0) {
-      prefetch_tensormap(&tmap_x);
-      const uint64_t pol = l2_policy_evict_first();
-      int i = 0;
       bool ok = true;
-      for (int r = 0; ok && kWG * r < n; ++r) {
-        const int act = min(kWG, n - kWG * r);
-        for (int c = 0; ok && c < kChunksPerSlice; c += kChunksPerStage) {
-          for (int g = 0; g < act; ++g, ++i) {
-            const int64_t unit = u_begin + kWG * r + g;
-            const int st = i % kXStages;
-            const uint32_t ph = (uint32_t)(i / kXStages) & 1u;
-            if (i >= kXStages &&
-                !mbar_wait(smem_u32(&bk.empty_x[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
-              fail(bk, err);
-              ok = false;
-              break;
-            }
-            const uint32_t full = smem_u32(&bk.full_x[st]);
-            mbar_arrive_expect_tx(full, kXTxBytes);
-            tma_load_3d(smem_u32(x_smem(st)), &tmap_x, 0, unit_tile(unit) * kTileM,
-                        unit_slice(unit) * kChunksPerSlice + c, full, pol);
-          }
-        }
-      }
+      const int i = x_loads(kXStages, 1 << 30, l2_policy_evict_first(), abort_flag, ok);
+      if (!ok) fail(bk, err);
       // drain: the loads still in flight complete before the CTA can exit
       for (int j = max(0, i - kXStages); j < i; ++j)
         mbar_wait(smem_u32(&bk.full_x[j % kXStages]), (uint32_t)(j / kXStages) & 1u, never,
