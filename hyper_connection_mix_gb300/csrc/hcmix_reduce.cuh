@@ -1,7 +1,7 @@
 // Ordered cross-slice reduction and the fused epilogue.
 //
 // The stock reduce+Sinkhorn kernel of the hc_fused page sums the per-slice
-// partials "in slice order" starting from zero and then runs the epilogue;
+// partials in slice order, starting from zero, and then runs the epilogue;
 // this kernel does the same from the workspace partials
 // part[(slice * 25 + j) * Mpad + row] (j < 24: mix, j = 24: sum of squares).
 //
