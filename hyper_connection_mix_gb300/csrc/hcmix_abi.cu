@@ -33,7 +33,6 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Workspace {
   size_t err_off = 0;     // uint32 device error word (256-byte header)
-  size_t gbar_off = 64;   // tensor-core grid barrier: count here, generation 64 bytes on
   size_t limbs_off = 0;   // packed W for the tensor-core path: bf16 limbs [4][24][K]
                           // (exact) or fp32 tf32x3 parts [2][24][K], the same size
   size_t limbs_bytes = 0;
@@ -131,8 +130,7 @@ hcmix_status launch_contraction(const void* x, int64_t x_stride, const float* W,
   if (path == HCMIX_PATH_TC || path == HCMIX_PATH_TC_TF32X3) {
     return tc_launch(static_cast<const uint16_t*>(x), x_stride, W, w_stride, M, K,
                      base + ws.limbs_off, part, (int)ws.Mpad,
-                     reinterpret_cast<uint32_t*>(base + ws.err_off),
-                     reinterpret_cast<uint32_t*>(base + ws.gbar_off), stream,
+                     reinterpret_cast<uint32_t*>(base + ws.err_off), stream,
                      path == HCMIX_PATH_TC_TF32X3);
   }
   return HCMIX_ERR_INVALID_ARG;
@@ -340,9 +338,7 @@ hcmix_status hc_mix_device_status(void* workspace, void* stream) {
   if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
     return HCMIX_ERR_CUDA;
   if (word != 0) {
-    // a kernel gave up part-way: clear the whole header, so that the grid
-    // barrier words start from zero again as well
-    if (cudaMemset(workspace, 0, kAlign) != cudaSuccess) return HCMIX_ERR_CUDA;
+    if (cudaMemset(workspace, 0, sizeof word) != cudaSuccess) return HCMIX_ERR_CUDA;
     return HCMIX_ERR_DEVICE;
   }
   return HCMIX_OK;

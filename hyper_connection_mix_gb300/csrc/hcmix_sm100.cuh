@@ -19,19 +19,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// ---------------------------------------------------------------- grid-wide ordering
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start once every CTA of the grid before it in the stream
+// has issued grid_launch_dependents (or exited); grid_dependency_wait then
+// blocks the calling thread until that earlier grid has completed and its
+// memory is visible.  Without such an earlier grid both return at once.
 
-// Acquire load of a global word at GPU scope.
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Orders this thread's generic-proxy global accesses before its later
-// async-proxy ones (TMA), and the reverse.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- shared memory

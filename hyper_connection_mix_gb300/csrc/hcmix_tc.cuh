@@ -122,29 +122,27 @@ static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynami
 static_assert(Mode<false>::kBBytes % 1024 == 0 && Mode<true>::kBBytes % 1024 == 0 &&
                   kLimbRowOffset + kLimbRows <= kBRows, "B buffer layout");
 
-// ---------------------------------------------------------------- W packing
-//
-// The contraction packs W itself: every CTA converts its share of W into the
-// workspace while its first x loads are in flight, and a grid-wide barrier
-// (all CTAs are co-resident: cooperative launch) releases the W producers'
-// TMA loads once every share is written.  A separate pack kernel ran to
-// completion before the contraction's CTAs could start, since its CTAs held
-// the registers a contraction CTA needs.
+// ---------------------------------------------------------------- W limbs
+
+// W[24, K] fp32 -> limbs[4][24][K] bf16 with W = w0 + w1 + w2 + w3 exactly:
+// w0 = W rounded to the grid 2^(ew-7) of its (output, chunk), then three
+// round-to-nearest bf16 pieces of the remainder.  16 lanes per (output,
+// chunk), four consecutive columns per lane.
+constexpr int kPackThreads = 256;
+constexpr int kPackTasksPerBlock = kPackThreads / 16;
 
 __device__ __forceinline__ uint32_t bf16_bits(float v) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
 }
 
-// One (output j, chunk c) task of the exact limbs, W[24, K] fp32 ->
-// limbs[4][24][K] bf16 with W = w0 + w1 + w2 + w3 exactly: w0 = W rounded to
-// the grid 2^(ew-7) of its (output, chunk), then three round-to-nearest bf16
-// pieces of the remainder.  16 lanes per task, four consecutive columns per
-// lane.  All 32 lanes of a warp call it together (the 16-lane maximum uses
-// shuffles); lanes whose task is not below task_end only take part in those.
-__device__ __forceinline__ void pack_limbs_task(const float* __restrict__ W, int64_t w_stride,
-                                                int K, uint16_t* __restrict__ limbs, int task,
-                                                int task_end, int nch, int sub) {
-  const bool active = task < task_end;
+__global__ void __launch_bounds__(kPackThreads)
+hcmix_pack_limbs_kernel(const float* __restrict__ W, int64_t w_stride, int K,
+                        uint16_t* __restrict__ limbs) {
+  sm100::grid_launch_dependents();  // the contraction may start streaming x now
+  const int sub = threadIdx.x & 15;
+  const int task = blockIdx.x * kPackTasksPerBlock + (threadIdx.x >> 4);
+  const int nch = K / kChunk;
+  const bool active = task < kMix * nch;
   const int j = active ? task / nch : 0, c = active ? task % nch : 0;
   const int64_t k = (int64_t)c * kChunk + 4 * sub;
   float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -178,13 +176,17 @@ __device__ __forceinline__ void pack_limbs_task(const float* __restrict__ W, int
         make_uint2(out[p][0], out[p][1]);
 }
 
-// One float4 (item i of [24][K / 4]) of the tf32x3 parts, W[24, K] fp32 ->
-// parts[2][24][K] fp32: part 0 is big = W rounded to tf32 (nearest, ties
-// away from zero), part 1 is small = W - big, exact in fp32 and passed to the
-// MMAs as it is (the page hands the unrounded difference to its tf32 dot).
-__device__ __forceinline__ void pack_tf32_item(const float* __restrict__ W, int64_t w_stride,
-                                               int K, float* __restrict__ parts, int64_t i) {
+// W[24, K] fp32 -> parts[2][24][K] fp32 for the tf32x3 mode: part 0 is
+// big = W rounded to tf32 (nearest, ties away from zero), part 1 is
+// small = W - big, exact in fp32 and passed to the MMAs as it is (the page
+// hands the unrounded difference to its tf32 dot).  One float4 per thread.
+__global__ void __launch_bounds__(kPackThreads)
+hcmix_pack_tf32_kernel(const float* __restrict__ W, int64_t w_stride, int K,
+                       float* __restrict__ parts) {
+  sm100::grid_launch_dependents();  // the contraction may start streaming x now
   const int64_t per_row = K / 4;
+  const int64_t i = (int64_t)blockIdx.x * kPackThreads + threadIdx.x;
+  if (i >= kMix * per_row) return;
   const int j = (int)(i / per_row);
   const int64_t k = (i % per_row) * 4;
   const float4 v = *reinterpret_cast<const float4*>(W + (int64_t)j * w_stride + k);
@@ -194,33 +196,6 @@ __device__ __forceinline__ void pack_tf32_item(const float* __restrict__ W, int6
                                    __fsub_rn(v.z, big.z), __fsub_rn(v.w, big.w));
   *reinterpret_cast<float4*>(parts + (int64_t)j * K + k) = big;
   *reinterpret_cast<float4*>(parts + (int64_t)(kMix + j) * K + k) = small;
-}
-
-// Grid-wide barrier on two words of the workspace header, count and
-// generation, called by one thread per CTA.  The last CTA to arrive resets
-// the count and advances the generation; the others wait, bounded, for the
-// generation to move.  Afterwards this thread's TMA loads see every CTA's
-// packed W.
-__device__ __forceinline__ bool grid_barrier(uint32_t* count, uint32_t* gen,
-                                             const volatile int* abort, uint64_t limit_ns) {
-  const uint32_t g0 = sm100::ld_acquire_gpu(gen);
-  __threadfence();
-  if (atomicAdd(count, 1u) + 1u == gridDim.x) {
-    atomicExch(count, 0u);
-    __threadfence();
-    atomicAdd(gen, 1u);
-  } else {
-    const uint64_t t0 = sm100::global_timer_ns();
-    for (uint32_t i = 1; sm100::ld_acquire_gpu(gen) == g0; ++i) {
-      if ((i & 63u) == 0) {
-        if (*abort) return false;
-        if (sm100::global_timer_ns() - t0 > limit_ns) return false;
-      }
-    }
-  }
-  __threadfence();
-  sm100::fence_proxy_async_global();
-  return true;
 }
 
 // ---------------------------------------------------------------- main kernel
@@ -397,9 +372,7 @@ template <bool kTf32>
 __global__ void __launch_bounds__(kThreads, 1)
 hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, int n_tiles, int Mpad,
-                int64_t n_units, float* __restrict__ part, uint32_t* __restrict__ err,
-                const float* __restrict__ W, int64_t w_stride, int K, void* __restrict__ packed,
-                uint32_t* __restrict__ gbar) {
+                int64_t n_units, float* __restrict__ part, uint32_t* __restrict__ err) {
   using namespace sm100;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -476,23 +449,6 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     bool ok = true;
     x_loads(0, kXStages, l2_policy_evict_first(), &bk.never, ok);
   }
-  // this CTA's share of the W packing (every thread), made visible to the
-  // other CTAs' TMA loads before the grid barrier
-  if constexpr (kTf32) {
-    const int64_t n_items = (int64_t)kMix * (K / 4);
-    for (int64_t i = b * n_items / G + threadIdx.x; i < (b + 1) * n_items / G; i += kThreads)
-      pack_tf32_item(W, w_stride, K, static_cast<float*>(packed), i);
-  } else {
-    const int nch = K / kChunk;
-    const int64_t n_tasks = (int64_t)kMix * nch;
-    const int t_begin = (int)(b * n_tasks / G), t_end = (int)((b + 1) * n_tasks / G);
-    constexpr int kGroups = kThreads / 16;  // 16 lanes per task
-    for (int t = t_begin; t < t_end; t += kGroups)  // same trip count for the whole CTA
-      pack_limbs_task(W, w_stride, K, static_cast<uint16_t*>(packed), t + (threadIdx.x >> 4),
-                      t_end, nch, threadIdx.x & 15);
-  }
-  __threadfence();
-  fence_proxy_async_global();
   if constexpr (!kTf32) {
     // rows 0..23 of each B buffer stay zero (the limbs are loaded to rows 24..119;
     // the tf32x3 boxes bring their own zero rows)
@@ -533,12 +489,10 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // last use)
     if (lane == 0) {
       prefetch_tensormap(&tmap_w);
+      grid_dependency_wait();  // the limbs come from the pack kernel launched before
       const uint64_t pol = l2_policy_evict_last();
       int loads[kWG] = {0, 0}, cur[kWG] = {-1, -1};
-      // every CTA's share of the packed W is written (every thread of this
-      // CTA passed the set-up barrier after its share)
-      bool ok = grid_barrier(gbar, gbar + 16, abort_flag, kWaitLimitNs);
-      if (!ok) fail(bk, err);
+      bool ok = true;
       for (int r = 0; ok && kWG * r < n; ++r) {
         const int act = min(kWG, n - kWG * r);
 #pragma unroll
@@ -877,8 +831,7 @@ inline bool make_map_tf32_parts(CUtensorMap* map, const float* parts, uint64_t K
 
 template <bool kTf32>
 hcmix_status launch_main(const CUtensorMap& mx, const CUtensorMap& mw, int64_t M, int64_t K,
-                         float* part, int Mpad, uint32_t* err, const float* W, int64_t w_stride,
-                         void* packed, uint32_t* gbar, cudaStream_t stream) {
+                         float* part, int Mpad, uint32_t* err, cudaStream_t stream) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -889,49 +842,56 @@ hcmix_status launch_main(const CUtensorMap& mx, const CUtensorMap& mw, int64_t M
   if (cudaFuncSetAttribute(hcmix_tc_kernel<kTf32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes<kTf32>) != cudaSuccess)
     return HCMIX_ERR_CUDA;
-  // cooperative: every CTA is resident at once, which the grid barrier after
-  // the in-kernel W packing needs (one CTA per SM, at most one per SM)
+  // launched as a programmatic dependent of the pack kernel: x streams while
+  // W is being packed; the W producer waits for the pack grid
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes<kTf32>;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, hcmix_tc_kernel<kTf32>, mx, mw, (int)n_tiles, Mpad, n_units, part,
-                         err, W, w_stride, (int)K, packed, gbar) != cudaSuccess)
+                         err) != cudaSuccess)
     return HCMIX_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
 }
 
 }  // namespace tc
 
-// The tensor-core contraction into `part`, packing W (exact limbs, or the
-// tf32x3 big / small parts) on the way.  `packed` is the workspace area of
-// 4 * 24 * K * 2 bytes (= 2 * 24 * K * 4) that receives the packed W; gbar
-// points at the two grid-barrier words of the workspace header (gbar[0] and
-// gbar[16], zero before the first call).
+// Packs W (exact limbs, or the tf32x3 big / small parts), then runs the
+// tensor-core contraction into `part`.  `packed` is the workspace area of
+// 4 * 24 * K * 2 bytes (= 2 * 24 * K * 4) that holds the packed W.
 inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* W,
                               int64_t w_stride, int64_t M, int64_t K, void* packed,
-                              float* part, int Mpad, uint32_t* err, uint32_t* gbar,
-                              cudaStream_t stream, bool tf32x3) {
+                              float* part, int Mpad, uint32_t* err, cudaStream_t stream,
+                              bool tf32x3) {
   CUtensorMap mx, mw;
   if (!tc::make_map_bf16_3d_chunks(&mx, x, (uint64_t)K, (uint64_t)M, (uint64_t)x_stride * 2,
                                     tc::kTileM, tc::kChunksPerStage))
     return HCMIX_ERR_CUDA;
   if (tf32x3) {
-    if (!tc::make_map_tf32_parts(&mw, static_cast<const float*>(packed), (uint64_t)K))
-      return HCMIX_ERR_CUDA;
-    return tc::launch_main<true>(mx, mw, M, K, part, Mpad, err, W, w_stride, packed, gbar,
-                                 stream);
+    float* parts = static_cast<float*>(packed);
+    const int64_t n4 = kMix * (K / 4);
+    tc::hcmix_pack_tf32_kernel<<<(unsigned)((n4 + tc::kPackThreads - 1) / tc::kPackThreads),
+                                 tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K, parts);
+    if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
+    if (!tc::make_map_tf32_parts(&mw, parts, (uint64_t)K)) return HCMIX_ERR_CUDA;
+    return tc::launch_main<true>(mx, mw, M, K, part, Mpad, err, stream);
   }
-  if (!tc::make_map_bf16_2d(&mw, packed, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
+  uint16_t* limbs = static_cast<uint16_t*>(packed);
+  const int nch = (int)(K / kChunk);
+  const int pack_blocks = (kMix * nch + tc::kPackTasksPerBlock - 1) / tc::kPackTasksPerBlock;
+  tc::hcmix_pack_limbs_kernel<<<pack_blocks, tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K,
+                                                                           limbs);
+  if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
+  if (!tc::make_map_bf16_2d(&mw, limbs, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
                             tc::kLimbRows))
     return HCMIX_ERR_CUDA;
-  return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, W, w_stride, packed, gbar, stream);
+  return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, stream);
 }
 
 }  // namespace hcmix

@@ -91,12 +91,9 @@ typedef enum {
 
 /* Bytes of device workspace that hc_mix_stats / hc_mix_fused need for M rows.
  * The workspace must be 256-byte aligned and zeroed once before its first use
- * (its first 256 bytes hold the device error word and the two words of the
- * tensor-core kernel's grid-wide barrier, which every call leaves at zero and
- * at its next generation); after that every call writes what it reads, so no
- * per-call clearing is needed.  A workspace sized for M rows serves any
- * smaller M.  Calls that share a workspace must not overlap on the GPU (issue
- * them on one stream).  Returns 0 for unsupported (K, mix). */
+ * (its first 256 bytes hold the device error word); after that every call
+ * writes what it reads, so no per-call clearing is needed.  A workspace sized
+ * for M rows serves any smaller M.  Returns 0 for unsupported (K, mix). */
 size_t hc_mix_workspace_bytes(int64_t M, int64_t K, int mix);
 
 /* mix_out[M, mix] (fp32) and sq_out[M] (fp32): the contraction and the sum of
@@ -187,9 +184,8 @@ hcmix_status hc_mix_fused_noalloc(const void* x, int64_t x_stride, const float* 
                                   float* pre, float* post, float* comb,
                                   float* mix_out, float* sq_out, void* stream);
 
-/* Synchronises `stream`, then reads the device error word that kernels set in
- * `workspace` when a bounded wait runs out; when it is set, clears the whole
- * 256-byte header (error word and grid-barrier words).  HCMIX_OK when clean,
+/* Synchronises `stream`, then reads and clears the device error word that
+ * kernels set in `workspace` when a bounded wait runs out.  HCMIX_OK when clean,
  * HCMIX_ERR_DEVICE when a kernel recorded an error, HCMIX_ERR_CUDA when the
  * stream reports a CUDA error. */
 hcmix_status hc_mix_device_status(void* workspace, void* stream);
