@@ -93,7 +93,9 @@ typedef enum {
  * The workspace must be 256-byte aligned and zeroed once before its first use
  * (its first 256 bytes hold the device error word); after that every call
  * writes what it reads, so no per-call clearing is needed.  A workspace sized
- * for M rows serves any smaller M.  Returns 0 for unsupported (K, mix). */
+ * for M rows serves any smaller M.  Calls that share a workspace must not
+ * overlap on the GPU (issue them on one stream).  Returns 0 for unsupported
+ * (K, mix). */
 size_t hc_mix_workspace_bytes(int64_t M, int64_t K, int mix);
 
 /* mix_out[M, mix] (fp32) and sq_out[M] (fp32): the contraction and the sum of
