@@ -46,6 +46,16 @@ def test_workspace_bytes(L):
     assert binding.workspace_bytes(-1, K) == 0
 
 
+def test_path_enum_matches_binding():
+    """The binding's path names carry the values hcmix_path declares."""
+    src = open(os.path.join(ROOT, "include", "hcmix.h")).read()
+    body = re.search(r"typedef enum \{([^}]*)\} hcmix_path;", src).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    declared = {m.group(1).lower(): int(m.group(2))
+                for m in re.finditer(r"HCMIX_PATH_(\w+)\s*=\s*(\d+)", body)}
+    assert declared == binding.PATHS
+
+
 def test_status_strings(L):
     for code, name in binding.STATUS.items():
         assert binding.hc_mix_status_string(code).startswith(name)
@@ -72,6 +82,8 @@ def test_host_validation_rejects_before_launch(L):
     assert _stats(L, wkb=1024) == 4          # workspace too small
     assert _stats(L, x=None) == 1
     assert _stats(L, path=7) == 1
+    assert _stats(L, path=5) == 1            # one past the last declared path
+    assert _stats(L, path=-1) == 1
     assert _stats(L, mo=None) == 1
     assert _stats(L, M=0, x=None, W=None, wk=None) == 0  # empty: nothing to do
 
