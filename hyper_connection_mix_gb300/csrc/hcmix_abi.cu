@@ -28,6 +28,10 @@ constexpr int64_t kMaxM = (int64_t(1) << 31) - 1;
 // 1 (14.8 us against 22.8 us at M = 1, 14.7 against 35.9 at M = 64), so AUTO
 // always takes it; the CUDA-core kernel stays available by name.
 constexpr int64_t kSimtMaxRows = 0;
+// Batches up to this many rows are reduced by hcmix_reduce_small_kernel (all
+// 32 lanes of a warp fetch one output's slices at once); above it the
+// one-lane-per-row kernel, whose loads are coalesced across rows, is used.
+constexpr int64_t kReduceSmallMaxM = 16;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -97,6 +101,17 @@ hcmix_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
 }
 
+// The CUDA-core kernels stage a whole slice in dynamic shared memory (over
+// the 48 KB default).
+hcmix_status simt_smem_attributes() {
+  if (cudaFuncSetAttribute(hcmix_simt_slice_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSimtSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(hcmix_simt_fullk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSimtSmemBytes) != cudaSuccess)
+    return HCMIX_ERR_CUDA;
+  return HCMIX_OK;
+}
+
 bool valid_path(hcmix_path path) {
   return path == HCMIX_PATH_AUTO || path == HCMIX_PATH_SIMT || path == HCMIX_PATH_TC ||
          path == HCMIX_PATH_SIMT_FULLK || path == HCMIX_PATH_TC_TF32X3;
@@ -117,13 +132,15 @@ hcmix_status launch_contraction(const void* x, int64_t x_stride, const float* W,
   path = resolve_path(path, M);
   if (path == HCMIX_PATH_SIMT) {
     dim3 grid((unsigned)((M + kSimtRows - 1) / kSimtRows), (unsigned)ws.n_slices);
-    hcmix_simt_slice_kernel<<<grid, kSimtThreads, 0, stream>>>(
+    if (simt_smem_attributes() != HCMIX_OK) return HCMIX_ERR_CUDA;
+    hcmix_simt_slice_kernel<<<grid, kSimtThreads, kSimtSmemBytes, stream>>>(
         static_cast<const uint16_t*>(x), x_stride, W, w_stride, (int)M, (int)ws.Mpad, part);
     return launch_status();
   }
   if (path == HCMIX_PATH_SIMT_FULLK) {
-    hcmix_simt_fullk_kernel<<<(unsigned)((M + kSimtRows - 1) / kSimtRows), kSimtThreads, 0,
-                              stream>>>(static_cast<const uint16_t*>(x), x_stride, W, w_stride,
+    if (simt_smem_attributes() != HCMIX_OK) return HCMIX_ERR_CUDA;
+    hcmix_simt_fullk_kernel<<<(unsigned)((M + kSimtRows - 1) / kSimtRows), kSimtThreads,
+                              kSimtSmemBytes, stream>>>(static_cast<const uint16_t*>(x), x_stride, W, w_stride,
                                         (int)M, (int)ws.Mpad, (int)ws.n_slices, part);
     return launch_status();
   }
@@ -148,6 +165,13 @@ hcmix_status launch_reduce(int64_t M, int64_t K, void* workspace, const float* h
   const float* part =
       reinterpret_cast<const float*>(static_cast<const char*>(workspace) + ws.part_off);
   const float inv_k = (float)(1.0 / (double)K);
+  if (M <= kReduceSmallMaxM && stored_slices <= kReduceSmallMaxSlices) {
+    hcmix_reduce_small_kernel<<<(unsigned)((M + kReduceSmallRows - 1) / kReduceSmallRows),
+                                kReduceThreads, 0, stream>>>(
+        part, stored_slices, (int)ws.Mpad, (int)M, inv_k, hc_scale, hc_base, iters, rms_eps,
+        hc_eps, pre, post, comb, mix_out, sq_out, do_epilogue);
+    return launch_status();
+  }
   dim3 grid((unsigned)((M + kReduceRows - 1) / kReduceRows));
   hcmix_reduce_kernel<<<grid, kReduceThreads, 0, stream>>>(
       part, stored_slices, (int)ws.Mpad, (int)M, inv_k, hc_scale, hc_base, iters, rms_eps,
@@ -319,7 +343,8 @@ hcmix_status hc_mix_fused_noalloc(const void* x, int64_t x_stride, const float* 
   float* part = static_cast<float*>(scratch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid((unsigned)((M + kSimtRows - 1) / kSimtRows), (unsigned)n_slices);
-  hcmix_simt_slice_kernel<<<grid, kSimtThreads, 0, s>>>(
+  if (simt_smem_attributes() != HCMIX_OK) return HCMIX_ERR_CUDA;
+  hcmix_simt_slice_kernel<<<grid, kSimtThreads, kSimtSmemBytes, s>>>(
       static_cast<const uint16_t*>(x), x_stride, W, w_stride, (int)M, (int)Mpad, part);
   st = launch_status();
   if (st != HCMIX_OK) return st;

@@ -24,15 +24,17 @@ constexpr int kReduceBatch = 40;
 // (s_tot[j][r]: j < 24 mix, j = 24 sum of squares): 16 threads per row,
 // thread e owns comb entry e = 4i + j and, for e < 8, logit e of pre (e < 4)
 // or post.  Sinkhorn sums are gathered with shuffles and added in index
-// order, as one thread per row would.  Threads 512 and up do nothing.
+// order, as one thread per row would.  The CTA's first nrows rows are done
+// (nrows <= 32 and nrows * 16 a multiple of 32, so that whole warps take
+// part in the shuffles); threads nrows * 16 and up do nothing.
 __device__ __forceinline__ void epilogue16(const float (&s_tot)[kPartStride][kReduceRows + 1],
-                                           int row0, int M, float inv_k,
+                                           int row0, int nrows, int M, float inv_k,
                                            const float* __restrict__ hc_scale,
                                            const float* __restrict__ hc_base, int iters,
                                            float rms_eps, float hc_eps, float* __restrict__ pre,
                                            float* __restrict__ post, float* __restrict__ comb) {
   const int tid = threadIdx.x;
-  if (tid >= kReduceRows * kHc * kHc) return;
+  if (tid >= nrows * kHc * kHc) return;
   const int rloc = tid >> 4, e = tid & 15;
   const int row = row0 + rloc;
   const int gbase = threadIdx.x & 16;  // first lane of this row's 16-lane group
@@ -100,7 +102,58 @@ hcmix_reduce_kernel(const float* __restrict__ part, int n_slices, int Mpad, int 
   }
   if (sq_out != nullptr && tid < kReduceRows && row0 + tid < M) sq_out[row0 + tid] = s_tot[kMix][tid];
   if (!do_epilogue) return;
-  epilogue16(s_tot, row0, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post, comb);
+  epilogue16(s_tot, row0, kReduceRows, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post, comb);
+}
+
+// Small-M variant (decode batches): 2 rows per CTA and one warp per output j.
+// All 32 lanes fetch the (row, j) values of the slices they own (slice s to
+// lane s % 32), so every load of a CTA is in flight at once; the values are
+// parked in shared memory and lane r of the warp then adds row r's slices in
+// slice order from zero.  Then the same 16-threads-per-row epilogue.
+constexpr int kReduceSmallRows = 2;
+constexpr int kReduceSmallMaxSlices = 128;  // slices held in shared memory (K <= 32768)
+
+__global__ void __launch_bounds__(kReduceThreads)
+hcmix_reduce_small_kernel(const float* __restrict__ part, int n_slices, int Mpad, int M,
+                          float inv_k, const float* __restrict__ hc_scale,
+                          const float* __restrict__ hc_base, int iters, float rms_eps,
+                          float hc_eps, float* __restrict__ pre, float* __restrict__ post,
+                          float* __restrict__ comb, float* __restrict__ mix_out,
+                          float* __restrict__ sq_out, int do_epilogue) {
+  __shared__ float s_val[kPartStride][kReduceSmallRows][kReduceSmallMaxSlices];
+  __shared__ float s_tot[kPartStride][kReduceRows + 1];
+  const int lane = threadIdx.x & 31, out = threadIdx.x >> 5;  // out: mix index or 24 (sq)
+  const int row0 = blockIdx.x * kReduceSmallRows;
+  const int64_t step = (int64_t)kPartStride * Mpad;
+#pragma unroll
+  for (int r = 0; r < kReduceSmallRows; ++r) {
+    if (row0 + r >= M) continue;
+    const float* p = part + (int64_t)out * Mpad + row0 + r;
+    float v[kReduceSmallMaxSlices / 32];
+#pragma unroll
+    for (int i = 0; i < kReduceSmallMaxSlices / 32; ++i) {
+      const int sl = lane + 32 * i;
+      v[i] = sl < n_slices ? __ldg(p + (int64_t)sl * step) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < kReduceSmallMaxSlices / 32; ++i) s_val[out][r][lane + 32 * i] = v[i];
+  }
+  __syncwarp();
+  float t = 0.0f;
+  if (lane < kReduceSmallRows && row0 + lane < M)
+    for (int sl = 0; sl < n_slices; ++sl) t = __fadd_rn(t, s_val[out][lane][sl]);
+  if (lane < kReduceSmallRows) s_tot[out][lane] = t;
+  __syncthreads();
+  const int tid = threadIdx.x;
+  if (mix_out != nullptr && tid < kReduceSmallRows * kMix) {
+    const int r = tid / kMix, jj = tid % kMix;
+    if (row0 + r < M) mix_out[(int64_t)(row0 + r) * kMix + jj] = s_tot[jj][r];
+  }
+  if (sq_out != nullptr && tid < kReduceSmallRows && row0 + tid < M)
+    sq_out[row0 + tid] = s_tot[kMix][tid];
+  if (!do_epilogue) return;
+  epilogue16(s_tot, row0, kReduceSmallRows, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps,
+             pre, post, comb);
 }
 
 // The epilogue alone from caller-provided mix[M, 24] and sq[M]: 32 rows per
@@ -124,7 +177,7 @@ hcmix_epilogue_kernel(const float* __restrict__ mix, const float* __restrict__ s
   if (threadIdx.x < kReduceRows)
     s_tot[kMix][threadIdx.x] = (int)threadIdx.x < rows ? sq[row0 + threadIdx.x] : 0.0f;
   __syncthreads();
-  epilogue16(s_tot, row0, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post, comb);
+  epilogue16(s_tot, row0, kReduceRows, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post, comb);
 }
 
 }  // namespace hcmix

@@ -301,6 +301,31 @@ def test_tf32x3_exact_on_grid_inputs(tf32x3):
     assert np.array_equal(got[3].astype(np.float64), exact), "tf32x3 grid inputs not exact"
 
 
+def test_tf32x3_strided_and_decode_sizes(tf32x3):
+    """Row pitches wider than K (x and W views of wider buffers) and the
+    decode sizes, held to the same bound; the run is repeatable bit for bit."""
+    K, M = 1024, 70
+    rng = np.random.default_rng(8)
+    xs = hi.bf16_bits_from_f64(rng.standard_normal((M, K + 64)))
+    Wf = (rng.standard_normal((24, K + 32)) * 0.03).astype(np.float32)
+    x, W = np.ascontiguousarray(xs[:, :K]), np.ascontiguousarray(Wf[:, :K])
+    want_mix, want_sq = oracle.stats(x, W)
+    out = binding.hc_mix_stats(dev_x(xs)[:, :K], dev(Wf)[:, :K], path=tf32x3)
+    torch.cuda.synchronize()
+    mix, sq = (o.cpu().numpy() for o in out)
+    assert (np.abs(mix.astype(np.float64) - want_mix) <= tf32x3_bound(x, W)).all()
+    assert np.array_equal(sq, want_sq)
+    xd, Wd = hi.make_x(256), hi.make_w()
+    for Md in (1, 4, 64, 256):
+        xm = np.ascontiguousarray(xd[:Md])
+        want_mix, want_sq = oracle.stats(xm, Wd, threads=THREADS)
+        a = [o.cpu().numpy() for o in binding.hc_mix_stats(dev_x(xm), dev(Wd), path=tf32x3)]
+        b = [o.cpu().numpy() for o in binding.hc_mix_stats(dev_x(xm), dev(Wd), path=tf32x3)]
+        assert (np.abs(a[0].astype(np.float64) - want_mix) <= tf32x3_bound(xm, Wd)).all(), Md
+        assert np.array_equal(a[1], want_sq), Md
+        assert all(np.array_equal(u, v) for u, v in zip(a, b)), f"M={Md} not repeatable"
+
+
 def test_tf32x3_is_not_auto():
     assert binding.hc_mix_auto_path(4096) != "tc_tf32x3"
     assert binding.hc_mix_auto_path(1) != "tc_tf32x3"
