@@ -135,26 +135,22 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
 }
 
-__global__ void __launch_bounds__(kPackThreads)
-hcmix_pack_limbs_kernel(const float* __restrict__ W, int64_t w_stride, int K,
-                        uint16_t* __restrict__ limbs) {
-  sm100::grid_launch_dependents();  // the contraction may start streaming x now
-  const int sub = threadIdx.x & 15;
-  const int task = blockIdx.x * kPackTasksPerBlock + (threadIdx.x >> 4);
-  const int nch = K / kChunk;
-  const bool active = task < kMix * nch;
-  const int j = active ? task / nch : 0, c = active ? task % nch : 0;
-  const int64_t k = (int64_t)c * kChunk + 4 * sub;
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (active) v = *reinterpret_cast<const float4*>(W + (int64_t)j * w_stride + k);
+// Largest |W| bit pattern over a 16-lane group's 64 values (four per lane);
+// every lane of the warp takes part.
+__device__ __forceinline__ uint32_t max_abs_bits16(float4 v) {
   uint32_t m = max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
                    max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu));
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (!active) return;
+  return m;
+}
+
+// The four bf16 limbs of four consecutive W values of one (output, chunk)
+// whose largest |W| has the bit pattern m: out[p] holds limb p of the four
+// values as two packed bf16 pairs.
+__device__ __forceinline__ void split_limbs4(float4 v, uint32_t m, uint32_t (&out)[4][2]) {
   const float magic = grid_magic_from_exp_field(m >> 23);
   const float in[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out[4][2];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float w0 = grid_round(in[e], magic);
@@ -170,6 +166,24 @@ hcmix_pack_limbs_kernel(const float* __restrict__ W, int64_t w_stride, int K,
       else out[p][e / 2] |= b[p] << 16;
     }
   }
+}
+
+__global__ void __launch_bounds__(kPackThreads)
+hcmix_pack_limbs_kernel(const float* __restrict__ W, int64_t w_stride, int K,
+                        uint16_t* __restrict__ limbs) {
+  sm100::grid_launch_dependents();  // the contraction may start streaming x now
+  const int sub = threadIdx.x & 15;
+  const int task = blockIdx.x * kPackTasksPerBlock + (threadIdx.x >> 4);
+  const int nch = K / kChunk;
+  const bool active = task < kMix * nch;
+  const int j = active ? task / nch : 0, c = active ? task % nch : 0;
+  const int64_t k = (int64_t)c * kChunk + 4 * sub;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (active) v = *reinterpret_cast<const float4*>(W + (int64_t)j * w_stride + k);
+  const uint32_t m = max_abs_bits16(v);
+  if (!active) return;
+  uint32_t out[4][2];
+  split_limbs4(v, m, out);
 #pragma unroll
   for (int p = 0; p < 4; ++p)
     *reinterpret_cast<uint2*>(limbs + ((int64_t)p * kMix + j) * K + k) =
@@ -372,7 +386,8 @@ template <bool kTf32>
 __global__ void __launch_bounds__(kThreads, 1)
 hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, int n_tiles, int Mpad,
-                int64_t n_units, float* __restrict__ part, uint32_t* __restrict__ err) {
+                int64_t n_units, float* __restrict__ part, uint32_t* __restrict__ err,
+                const float* __restrict__ w_src, int64_t w_stride) {
   using namespace sm100;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -457,6 +472,48 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       const int s = idx / kUnits, u = idx % kUnits;
       sts128(smem_u32(b_smem(s)) + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
     }
+    if (w_src != nullptr) {
+      // every CTA owns one unit (small batches): the whole CTA splits that
+      // unit's slice of W straight into warpgroup 0's four B buffers, in the
+      // layout the TMA would give (row r of a buffer: 128 bytes, 16-byte
+      // piece i stored at piece i ^ (r & 7)), instead of a separate pack
+      // kernel writing limbs for every slice
+      const int64_t k_slice = (int64_t)(u_begin / n_tiles) * kSlice;
+      const int sub = threadIdx.x & 15;
+      constexpr int kTasks = kMix * kChunksPerSlice;  // (output, chunk) pairs, 16 lanes each
+      constexpr int kGroups = kThreads / 16;
+      constexpr int kRounds = (kTasks + kGroups - 1) / kGroups;
+      float4 wv[kRounds];  // every W load of this lane in flight at once
+#pragma unroll
+      for (int q = 0; q < kRounds; ++q) {
+        const int task = q * kGroups + (threadIdx.x >> 4);
+        wv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (task < kTasks)
+          wv[q] = *reinterpret_cast<const float4*>(
+              w_src + (int64_t)(task / kChunksPerSlice) * w_stride + k_slice +
+              (task % kChunksPerSlice) * kChunk + 4 * sub);
+      }
+#pragma unroll
+      for (int q = 0; q < kRounds; ++q) {  // uniform trip count
+        const int task = q * kGroups + (threadIdx.x >> 4);
+        const bool active = task < kTasks;
+        const int j = active ? task / kChunksPerSlice : 0, c = active ? task % kChunksPerSlice : 0;
+        const float4 v = wv[q];
+        const uint32_t m = max_abs_bits16(v);
+        if (!active) continue;
+        uint32_t out[4][2];
+        split_limbs4(v, m, out);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const uint32_t r = kLimbRowOffset + (uint32_t)(p * kMix + j);
+          const uint32_t addr = smem_u32(b_smem(c)) + r * kRowBytes +
+                                ((((uint32_t)sub >> 1) ^ (r & 7u)) << 4) + ((uint32_t)sub & 1u) * 8;
+          asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(out[p][0]),
+                       "r"(out[p][1])
+                       : "memory");
+        }
+      }
+    }
     fence_proxy_async_smem();
   }
   if (warp == 1) {
@@ -487,7 +544,10 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // four B buffers are reloaded with that slice's limbs, once the MMAs of
     // its previous slice have released them (empty_b, committed after their
     // last use)
-    if (lane == 0) {
+    if (lane == 0 && w_src != nullptr) {
+      // the set-up filled warpgroup 0's buffers with the CTA's only slice
+      for (int c = 0; c < kChunksPerSlice; ++c) mbar_arrive(smem_u32(&bk.full_b[c]));
+    } else if (lane == 0) {
       prefetch_tensormap(&tmap_w);
       grid_dependency_wait();  // the limbs come from the pack kernel launched before
       const uint64_t pol = l2_policy_evict_last();
@@ -831,7 +891,8 @@ inline bool make_map_tf32_parts(CUtensorMap* map, const float* parts, uint64_t K
 
 template <bool kTf32>
 hcmix_status launch_main(const CUtensorMap& mx, const CUtensorMap& mw, int64_t M, int64_t K,
-                         float* part, int Mpad, uint32_t* err, cudaStream_t stream) {
+                         float* part, int Mpad, uint32_t* err, const float* w_src,
+                         int64_t w_stride, bool dependent, cudaStream_t stream) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -853,9 +914,9 @@ hcmix_status launch_main(const CUtensorMap& mx, const CUtensorMap& mw, int64_t M
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = dependent ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, hcmix_tc_kernel<kTf32>, mx, mw, (int)n_tiles, Mpad, n_units, part,
-                         err) != cudaSuccess)
+                         err, w_src, w_stride) != cudaSuccess)
     return HCMIX_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
 }
@@ -880,18 +941,25 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
                                  tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K, parts);
     if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
     if (!tc::make_map_tf32_parts(&mw, parts, (uint64_t)K)) return HCMIX_ERR_CUDA;
-    return tc::launch_main<true>(mx, mw, M, K, part, Mpad, err, stream);
+    return tc::launch_main<true>(mx, mw, M, K, part, Mpad, err, nullptr, 0, true, stream);
   }
   uint16_t* limbs = static_cast<uint16_t*>(packed);
+  if (!tc::make_map_bf16_2d(&mw, limbs, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
+                            tc::kLimbRows))
+    return HCMIX_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return HCMIX_ERR_CUDA;
+  const int64_t n_units = (M + tc::kTileM - 1) / tc::kTileM * (K / kSlice);
+  if (n_units <= sms)  // one unit per CTA: each CTA splits its own slice of W
+    return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, W, w_stride, false, stream);
   const int nch = (int)(K / kChunk);
   const int pack_blocks = (kMix * nch + tc::kPackTasksPerBlock - 1) / tc::kPackTasksPerBlock;
   tc::hcmix_pack_limbs_kernel<<<pack_blocks, tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K,
                                                                            limbs);
   if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
-  if (!tc::make_map_bf16_2d(&mw, limbs, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
-                            tc::kLimbRows))
-    return HCMIX_ERR_CUDA;
-  return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, stream);
+  return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, nullptr, 0, true, stream);
 }
 
 }  // namespace hcmix
