@@ -12,7 +12,10 @@
 //   * warp 0 (one thread) loads x with TMA, two chunks of a tile (32 KB) per
 //     load, into a 3-stage ring; warp 2 (one thread) loads the four W limbs of
 //     a slice [96 rows x 64 per chunk] into the B buffers of a warpgroup when
-//     that warpgroup reaches a new slice (128-byte swizzle for both);
+//     that warpgroup reaches a new slice (128-byte swizzle for both).  The
+//     limbs come from hcmix_pack_limbs_kernel, except when every CTA owns one
+//     unit (small batches): the CTA then splits its slice of W into the B
+//     buffers itself during set-up;
 //   * a compute warpgroup (one thread per row) reads its row from shared
 //     memory, sums the squares with the page's tree, splits x into the limbs
 //     x0 (grid-aligned) and x1 = x - x0, and stores both into its TMEM A area;
@@ -21,8 +24,9 @@
 //     against x0, accumulating into the warpgroup's TMEM D:
 //       D = [x0.w0 | x0.w1 + x1.w0 | x0.w2 + x1.w1 | x0.w3 + x1.w2]
 //     (the first 24 columns are exact; x1.w3 ~ 2^-34 relative is dropped);
-//     the whole warp runs the issue loop and one elected lane issues, which
-//     keeps the loop warp-uniform (twice the MMA rate of a one-lane loop);
+//     the whole warp runs the issue loop and one elected lane issues a
+//     chunk's MMAs and commit from one inline-assembly block, which keeps the
+//     loop warp-uniform and the issuer's instruction count small;
 //   * the warpgroup reads D and forms the chunk dot fl32(top + rest).
 // Two warpgroups work on two units at a time.  Each is software-pipelined: it
 // transforms chunk k+1 into its second TMEM A buffer before it waits for the
