@@ -22,7 +22,7 @@ Our arm prints one JSON line with:
 `--sweep` times the other workloads instead, one JSON line each: the decode
 sweep M in {1, 4, 16, 64, 128, 256} on both paths, M = 512 with outlier
 channels, the stock split-K / fused full-K A/B at M in {512, 1024, 2048, 4096},
-and one 86-call forward (M = 16384, distinct W / scale / base per
+the 4096-row call on a W packed once, and one 86-call forward (M = 16384, distinct W / scale / base per
 call) replayed from a single CUDA graph.
 Multi-GPU (torchrun): each rank runs its own 4096 rows (weak scaling, rows are
 independent, no collective on the data path).
@@ -506,6 +506,24 @@ def run_sweep(args):
                               "us_per_call": us,
                               "hbm_gbs": traffic.algorithmic_bytes(M, K_COLS) / (us * 1e-6) / 1e9}),
                   flush=True)
+
+    # W packed once (a layer's weight during inference): the same 4096-row
+    # call without the per-call conversion of W
+    x = torch.from_numpy(x4096.view(np.int16)).view(torch.bfloat16).to(device)
+    packed = binding.pack_w(W, stream=stream)
+    ws4 = binding.alloc_workspace(4096, K_COLS, device)
+    out4 = (torch.empty(4096, 4, device=device), torch.empty(4096, 4, device=device),
+            torch.empty(4096, 4, 4, device=device))
+
+    def packed_calls():
+        for _ in range(10):
+            binding.hc_mix_fused_packed(x, packed, sc, bs, ITERS, RMS_EPS, HC_EPS, out=out4,
+                                        workspace=ws4, stream=stream)
+    us = graph_us(packed_calls, stream, replays=10) / 10
+    print(json.dumps({"config": f"M=4096 K={K_COLS}, W packed once", "path": "tc (packed W)",
+                      "us_per_call": us,
+                      "hbm_gbs": traffic.algorithmic_bytes(4096, K_COLS) / (us * 1e-6) / 1e9}),
+          flush=True)
 
     # 86 calls per forward (43 layers x 2), M = 16384, one shared x, distinct
     # W / scale / base per call (the stack test's seeds), one CUDA graph

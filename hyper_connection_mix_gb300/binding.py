@@ -28,7 +28,8 @@ PATHS = {"auto": 0, "simt": 1, "tc": 2, "simt_fullk": 3, "tc_tf32x3": 4}
 # every symbol include/hcmix.h declares
 EXPORTS = ("hc_mix_workspace_bytes", "hc_mix_stats", "hc_mix_sinkhorn", "hc_mix_fused",
            "hc_mix_stats_ex", "hc_mix_fused_ex", "hc_mix_contract_ex", "hc_mix_auto_path",
-           "hc_mix_device_status", "hc_mix_status_string", "hc_mix_fused_noalloc")
+           "hc_mix_device_status", "hc_mix_status_string", "hc_mix_fused_noalloc",
+           "hc_mix_packed_w_bytes", "hc_mix_pack_w", "hc_mix_fused_packed")
 
 
 class HcMixError(RuntimeError):
@@ -71,6 +72,13 @@ def lib() -> ctypes.CDLL:
             L.hc_mix_fused_noalloc.restype = I
             L.hc_mix_fused_noalloc.argtypes = [P, I64, P, I64, I64, I64, I, I, P, P, I, F, F,
                                                P, P, P, P, P, P]
+            L.hc_mix_packed_w_bytes.restype = S
+            L.hc_mix_packed_w_bytes.argtypes = [I64, I]
+            L.hc_mix_pack_w.restype = I
+            L.hc_mix_pack_w.argtypes = [P, I64, I64, I, P, S, P]
+            L.hc_mix_fused_packed.restype = I
+            L.hc_mix_fused_packed.argtypes = [P, I64, P, S, I64, I64, I, I, P, P, I, F, F,
+                                              P, P, P, P, P, P, S, P]
             L.hc_mix_auto_path.restype = I
             L.hc_mix_auto_path.argtypes = [I64]
             L.hc_mix_device_status.restype = I
@@ -187,6 +195,45 @@ def hc_mix_contract(x: torch.Tensor, W: torch.Tensor, workspace: torch.Tensor, s
                                   _ptr(workspace), workspace.numel(), _stream(stream),
                                   PATHS[_auto(path, x.device)])
     _check(st, "hc_mix_contract")
+
+
+def pack_w(W: torch.Tensor, packed=None, stream=None) -> torch.Tensor:
+    """W[24, K] packed once into the tensor-core operand format (uint8 on W's
+    device, 256-byte aligned) for hc_mix_fused_packed."""
+    _check_w(W)
+    K = W.shape[1]
+    n = int(lib().hc_mix_packed_w_bytes(K, W.shape[0]))
+    if n == 0:
+        raise HcMixError(3, "hc_mix_packed_w_bytes")
+    packed = torch.empty(n, dtype=torch.uint8, device=W.device) if packed is None else packed
+    st = lib().hc_mix_pack_w(_ptr(W), W.stride(0), K, W.shape[0], _ptr(packed), packed.numel(),
+                             _stream(stream))
+    _check(st, "hc_mix_pack_w")
+    return packed
+
+
+def hc_mix_fused_packed(x: torch.Tensor, packed: torch.Tensor, hc_scale: torch.Tensor,
+                        hc_base: torch.Tensor, sinkhorn_iters: int = 20, rms_eps: float = 1e-6,
+                        hc_eps: float = 0.0, want_stats: bool = False, out=None, workspace=None,
+                        stream=None):
+    """hc_mix_fused on a W packed by pack_w (tensor-core path, exact limbs)."""
+    _check_x(x)
+    M, K = x.shape
+    dev = x.device
+    pre, post, comb = out if out is not None else (
+        torch.empty(M, HC, dtype=torch.float32, device=dev),
+        torch.empty(M, HC, dtype=torch.float32, device=dev),
+        torch.empty(M, HC, HC, dtype=torch.float32, device=dev))
+    mix_out = torch.empty(M, MIX, dtype=torch.float32, device=dev) if want_stats else None
+    sq_out = torch.empty(M, dtype=torch.float32, device=dev) if want_stats else None
+    workspace = alloc_workspace(M, K, dev) if workspace is None else workspace
+    st = lib().hc_mix_fused_packed(_ptr(x), x.stride(0), _ptr(packed), packed.numel(), M, K, MIX,
+                                   HC, _ptr(hc_scale), _ptr(hc_base), sinkhorn_iters, rms_eps,
+                                   hc_eps, _ptr(pre), _ptr(post), _ptr(comb), _ptr(mix_out),
+                                   _ptr(sq_out), _ptr(workspace), workspace.numel(),
+                                   _stream(stream))
+    _check(st, "hc_mix_fused_packed")
+    return (pre, post, comb, mix_out, sq_out) if want_stats else (pre, post, comb)
 
 
 def hc_mix_auto_path(M: int) -> str:

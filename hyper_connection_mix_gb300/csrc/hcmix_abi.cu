@@ -269,6 +269,53 @@ hcmix_status hc_mix_fused_ex(const void* x, int64_t x_stride, const float* W, in
                        post, comb, mix_out, sq_out, 1, s, path);
 }
 
+size_t hc_mix_packed_w_bytes(int64_t K, int mix) {
+  if (check_shape(0, K, mix) != HCMIX_OK) return 0;
+  return (size_t)4 * kMix * (size_t)K * 2;
+}
+
+hcmix_status hc_mix_pack_w(const float* W, int64_t w_stride, int64_t K, int mix, void* packed_w,
+                           size_t packed_bytes, void* stream) {
+  hcmix_status st = check_shape(0, K, mix);
+  if (st != HCMIX_OK) return st;
+  if (W == nullptr || packed_w == nullptr || w_stride < K) return HCMIX_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || (w_stride * 4) % 16 != 0 || !aligned(packed_w, kAlign))
+    return HCMIX_ERR_ALIGNMENT;
+  if (packed_bytes < hc_mix_packed_w_bytes(K, mix)) return HCMIX_ERR_WORKSPACE;
+  return tc_pack_limbs(W, w_stride, K, static_cast<uint16_t*>(packed_w),
+                       static_cast<cudaStream_t>(stream));
+}
+
+hcmix_status hc_mix_fused_packed(const void* x, int64_t x_stride, const void* packed_w,
+                                 size_t packed_bytes, int64_t M, int64_t K, int mix, int hc,
+                                 const float* hc_scale, const float* hc_base, int sinkhorn_iters,
+                                 float rms_eps, float hc_eps, float* pre, float* post,
+                                 float* comb, float* mix_out, float* sq_out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  hcmix_status st = check_shape(M, K, mix);
+  if (st != HCMIX_OK) return st;
+  st = check_epilogue_args(M, K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
+  if (st != HCMIX_OK) return st;
+  if (M == 0) return HCMIX_OK;
+  if (x == nullptr || packed_w == nullptr || workspace == nullptr || x_stride < K)
+    return HCMIX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (x_stride * 2) % 16 != 0 || !aligned(packed_w, kAlign) ||
+      !aligned(workspace, kAlign))
+    return HCMIX_ERR_ALIGNMENT;
+  if (packed_bytes < hc_mix_packed_w_bytes(K, mix) ||
+      workspace_bytes < workspace_layout(M, K).total)
+    return HCMIX_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Workspace ws = workspace_layout(M, K);
+  char* base = static_cast<char*>(workspace);
+  st = tc_launch(static_cast<const uint16_t*>(x), x_stride, nullptr, 0, M, K,
+                 const_cast<void*>(packed_w), reinterpret_cast<float*>(base + ws.part_off),
+                 (int)ws.Mpad, reinterpret_cast<uint32_t*>(base + ws.err_off), s, false);
+  if (st != HCMIX_OK) return st;
+  return launch_reduce(M, K, workspace, hc_scale, hc_base, sinkhorn_iters, rms_eps, hc_eps, pre,
+                       post, comb, mix_out, sq_out, 1, s, HCMIX_PATH_TC);
+}
+
 hcmix_status hc_mix_fused(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
                           int64_t M, int64_t K, int mix, int hc, const float* hc_scale,
                           const float* hc_base, int sinkhorn_iters, float rms_eps, float hc_eps,

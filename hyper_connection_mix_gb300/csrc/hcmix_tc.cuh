@@ -929,11 +929,14 @@ hcmix_status launch_main(const CUtensorMap& mx, const CUtensorMap& mw, int64_t M
 
 // Packs W (exact limbs, or the tf32x3 big / small parts), then runs the
 // tensor-core contraction into `part`.  `packed` is the workspace area of
-// 4 * 24 * K * 2 bytes (= 2 * 24 * K * 4) that holds the packed W.
+// 4 * 24 * K * 2 bytes (= 2 * 24 * K * 4) that holds the packed W.  With W
+// null (exact mode only), `packed` already holds limbs written by
+// hcmix_pack_limbs_kernel and nothing is packed.
 inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* W,
                               int64_t w_stride, int64_t M, int64_t K, void* packed,
                               float* part, int Mpad, uint32_t* err, cudaStream_t stream,
                               bool tf32x3) {
+  if (W == nullptr && tf32x3) return HCMIX_ERR_INVALID_ARG;  // prepacked W: exact limbs only
   CUtensorMap mx, mw;
   if (!tc::make_map_bf16_3d_chunks(&mx, x, (uint64_t)K, (uint64_t)M, (uint64_t)x_stride * 2,
                                     tc::kTileM, tc::kChunksPerStage))
@@ -951,6 +954,8 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
   if (!tc::make_map_bf16_2d(&mw, limbs, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
                             tc::kLimbRows))
     return HCMIX_ERR_CUDA;
+  if (W == nullptr)  // limbs packed ahead of the call
+    return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, nullptr, 0, false, stream);
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -964,6 +969,16 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
                                                                            limbs);
   if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
   return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, nullptr, 0, true, stream);
+}
+
+// W[24, K] fp32 -> limbs[4][24][K] bf16, the tensor-core kernel's B operand.
+inline hcmix_status tc_pack_limbs(const float* W, int64_t w_stride, int64_t K, uint16_t* limbs,
+                                  cudaStream_t stream) {
+  const int nch = (int)(K / kChunk);
+  const int pack_blocks = (kMix * nch + tc::kPackTasksPerBlock - 1) / tc::kPackTasksPerBlock;
+  tc::hcmix_pack_limbs_kernel<<<pack_blocks, tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K,
+                                                                           limbs);
+  return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
 }
 
 }  // namespace hcmix

@@ -150,6 +150,27 @@ hcmix_status hc_mix_contract_ex(const void* x, int64_t x_stride, const float* W,
                                 void* workspace, size_t workspace_bytes, void* stream,
                                 hcmix_path path);
 
+/* W packed once, for callers whose weight does not change between calls (a
+ * model layer's W during inference).  The hc_fused page has no counterpart:
+ * its kernel reads fp32 W on every call, and so do hc_mix_fused and
+ * hc_mix_stats, whose tensor-core path converts W into its MMA operand format
+ * each time.  hc_mix_pack_w does that conversion once into a caller buffer
+ * (packed_w, 256-byte aligned, hc_mix_packed_w_bytes(K, mix) bytes: the exact
+ * bf16 limbs W = w0 + w1 + w2 + w3, an opaque format tied to this library
+ * build), and hc_mix_fused_packed runs the tensor-core path (exact limbs) on
+ * it.  Its results are bit-identical to hc_mix_fused's tensor-core path on the
+ * same W.  Repack after W changes.  Other arguments, validation and error
+ * behaviour follow hc_mix_fused (x / workspace) and hc_mix_stats (W). */
+size_t hc_mix_packed_w_bytes(int64_t K, int mix);
+hcmix_status hc_mix_pack_w(const float* W, int64_t w_stride, int64_t K, int mix, void* packed_w,
+                           size_t packed_bytes, void* stream);
+hcmix_status hc_mix_fused_packed(const void* x, int64_t x_stride, const void* packed_w,
+                                 size_t packed_bytes, int64_t M, int64_t K, int mix, int hc,
+                                 const float* hc_scale, const float* hc_base, int sinkhorn_iters,
+                                 float rms_eps, float hc_eps, float* pre, float* post,
+                                 float* comb, float* mix_out, float* sq_out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* The path HCMIX_PATH_AUTO takes for M rows. */
 hcmix_path hc_mix_auto_path(int64_t M);
 

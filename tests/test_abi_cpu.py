@@ -56,6 +56,41 @@ def test_path_enum_matches_binding():
     assert declared == binding.PATHS
 
 
+def test_packed_w_validation(L):
+    """The pack-once entry points reject bad arguments before launching."""
+    K = 20480
+    assert binding.lib().hc_mix_packed_w_bytes(K, 24) == 4 * 24 * K * 2
+    assert binding.lib().hc_mix_packed_w_bytes(K, 16) == 0
+    assert binding.lib().hc_mix_packed_w_bytes(1000, 24) == 0
+    n = 4 * 24 * K * 2
+    pack = L.hc_mix_pack_w
+    assert pack(None, K, K, 24, 0x100000, n, None) == 1
+    assert pack(0x20000, K - 4, K, 24, 0x100000, n, None) == 1   # stride < K
+    assert pack(0x20004, K, K, 24, 0x100000, n, None) == 2       # W misaligned
+    assert pack(0x20000, K, K, 24, 0x100080, n, None) == 2       # packed not 256-byte aligned
+    assert pack(0x20000, K, K, 24, 0x100000, n - 1, None) == 4   # packed too small
+    assert pack(0x20000, K, 1000, 24, 0x100000, n, None) == 3
+    fp = L.hc_mix_fused_packed
+    P = 0x10000
+    args = dict(x=P, xs=K, pw=0x200000, pb=n, M=8, K=K, mix=24, hc=4, sc=P, bs=P, it=20,
+                re=1e-6, he=0.0, pre=P, post=P, comb=P, mo=None, so=None, wk=0x800000,
+                wkb=1 << 30)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return fp(a["x"], a["xs"], a["pw"], a["pb"], a["M"], a["K"], a["mix"], a["hc"], a["sc"],
+                  a["bs"], a["it"], a["re"], a["he"], a["pre"], a["post"], a["comb"], a["mo"],
+                  a["so"], a["wk"], a["wkb"], None)
+    assert call(pw=None) == 1
+    assert call(pw=0x200080) == 2
+    assert call(pb=n - 1) == 4
+    assert call(wkb=1024) == 4
+    assert call(x=0x10002) == 2
+    assert call(hc=3) == 3
+    assert call(it=-1) == 1
+    assert call(M=0, x=None, pw=None, wk=None) == 0
+
+
 def test_status_strings(L):
     for code, name in binding.STATUS.items():
         assert binding.hc_mix_status_string(code).startswith(name)

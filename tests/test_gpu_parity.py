@@ -331,6 +331,25 @@ def test_tf32x3_is_not_auto():
     assert binding.hc_mix_auto_path(1) != "tc_tf32x3"
 
 
+@pytest.mark.parametrize("M", [1, 130, 4096])
+def test_fused_packed_matches_fused(M):
+    """W packed once gives the tensor-core path's results bit for bit, and a
+    repacked buffer follows a new W."""
+    if not path_available("tc"):
+        pytest.fail("kernel path tc is not available in this library")
+    x = dev_x(hi.make_x(M, outliers=True))
+    sc, bs = dev(hi.make_scale()), dev(hi.make_base())
+    packed = None
+    for seed in (1, 7):
+        W = dev(hi.make_w(seed=seed))
+        packed = binding.pack_w(W, packed=packed)
+        a = binding.hc_mix_fused(x, W, sc, bs, want_stats=True, path="tc")
+        b = binding.hc_mix_fused_packed(x, packed, sc, bs, want_stats=True)
+        torch.cuda.synchronize()
+        for name, u, v in zip(("pre", "post", "comb", "mix", "sq"), a, b):
+            assert torch.equal(u.view(torch.int32), v.view(torch.int32)), f"seed {seed}: {name}"
+
+
 def test_stack86_m16384_sampled():
     """The 43-layer stack: 86 calls at M=16384 with distinct W / scale / base,
     captured once in a CUDA graph as the benchmark runs it.  Sampled rows of every
