@@ -126,14 +126,23 @@ def _check_w(W: torch.Tensor) -> None:
         raise ValueError("W must be a 2-D CUDA fp32 tensor with unit inner stride")
 
 
+def _f32(like: torch.Tensor, *shape) -> torch.Tensor:
+    """An uninitialised fp32 tensor of `shape` on `like`'s device."""
+    return like.new_empty(shape, dtype=torch.float32)
+
+
+def _hc_outputs(like: torch.Tensor, M: int):
+    """Output buffers (pre[M, 4], post[M, 4], comb[M, 4, 4]) on `like`'s device."""
+    return (_f32(like, M, HC), _f32(like, M, HC), _f32(like, M, HC, HC))
+
+
 def hc_mix_stats(x: torch.Tensor, W: torch.Tensor, mix_out=None, sq_out=None, workspace=None,
                  stream=None, path: str = "auto"):
     """(mix[M, 24], sq[M]) fp32 on x's device."""
     _check_x(x); _check_w(W)
     M, K = x.shape
-    mix_out = torch.empty(M, W.shape[0], dtype=torch.float32, device=x.device) \
-        if mix_out is None else mix_out
-    sq_out = torch.empty(M, dtype=torch.float32, device=x.device) if sq_out is None else sq_out
+    mix_out = _f32(x, M, W.shape[0]) if mix_out is None else mix_out
+    sq_out = _f32(x, M) if sq_out is None else sq_out
     workspace = alloc_workspace(M, K, x.device) if workspace is None else workspace
     st = lib().hc_mix_stats_ex(_ptr(x), x.stride(0), _ptr(W), W.stride(0), M, K, W.shape[0],
                                _ptr(mix_out), _ptr(sq_out), _ptr(workspace), workspace.numel(),
@@ -147,11 +156,7 @@ def hc_mix_sinkhorn(mix: torch.Tensor, sq: torch.Tensor, K: int, hc_scale: torch
                     hc_eps: float = 0.0, out=None, stream=None):
     """(pre[M, 4], post[M, 4], comb[M, 4, 4]) from mix[M, 24] and sq[M]."""
     M = mix.shape[0]
-    dev = mix.device
-    pre, post, comb = out if out is not None else (
-        torch.empty(M, HC, dtype=torch.float32, device=dev),
-        torch.empty(M, HC, dtype=torch.float32, device=dev),
-        torch.empty(M, HC, HC, dtype=torch.float32, device=dev))
+    pre, post, comb = out if out is not None else _hc_outputs(mix, M)
     st = lib().hc_mix_sinkhorn(_ptr(mix), _ptr(sq), M, K, mix.shape[1], HC, _ptr(hc_scale),
                                _ptr(hc_base), sinkhorn_iters, rms_eps, hc_eps, _ptr(pre),
                                _ptr(post), _ptr(comb), _stream(stream))
@@ -168,12 +173,9 @@ def hc_mix_fused(x: torch.Tensor, W: torch.Tensor, hc_scale: torch.Tensor,
     M, K = x.shape
     dev = x.device
     if out is None:
-        out = (torch.empty(M, HC, dtype=torch.float32, device=dev),
-               torch.empty(M, HC, dtype=torch.float32, device=dev),
-               torch.empty(M, HC, HC, dtype=torch.float32, device=dev))
+        out = _hc_outputs(x, M)
         if want_stats:
-            out += (torch.empty(M, W.shape[0], dtype=torch.float32, device=dev),
-                    torch.empty(M, dtype=torch.float32, device=dev))
+            out += (_f32(x, M, W.shape[0]), _f32(x, M))
     pre, post, comb = out[:3]
     mix_out, sq_out = (out[3], out[4]) if len(out) == 5 else (None, None)
     workspace = alloc_workspace(M, K, dev) if workspace is None else workspace
@@ -220,12 +222,9 @@ def hc_mix_fused_packed(x: torch.Tensor, packed: torch.Tensor, hc_scale: torch.T
     _check_x(x)
     M, K = x.shape
     dev = x.device
-    pre, post, comb = out if out is not None else (
-        torch.empty(M, HC, dtype=torch.float32, device=dev),
-        torch.empty(M, HC, dtype=torch.float32, device=dev),
-        torch.empty(M, HC, HC, dtype=torch.float32, device=dev))
-    mix_out = torch.empty(M, MIX, dtype=torch.float32, device=dev) if want_stats else None
-    sq_out = torch.empty(M, dtype=torch.float32, device=dev) if want_stats else None
+    pre, post, comb = out if out is not None else _hc_outputs(x, M)
+    mix_out = _f32(x, M, MIX) if want_stats else None
+    sq_out = _f32(x, M) if want_stats else None
     workspace = alloc_workspace(M, K, dev) if workspace is None else workspace
     st = lib().hc_mix_fused_packed(_ptr(x), x.stride(0), _ptr(packed), packed.numel(), M, K, MIX,
                                    HC, _ptr(hc_scale), _ptr(hc_base), sinkhorn_iters, rms_eps,

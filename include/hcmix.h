@@ -64,8 +64,8 @@ typedef enum {
  *
  * HCMIX_PATH_SIMT and HCMIX_PATH_SIMT_FULLK are the hc_fused page's two
  * designs on the same CUDA-core arithmetic, kept as an A/B pair: the stock
- * engine's split-K layout (one CTA per slice and row block, every slice's
- * totals stored in the workspace, then an ordered reduce) against the page's
+ * engine's split-K layout (each (slice, row block) pair gets a CTA of its own
+ * that writes its slice's totals to the workspace; an ordered reduce follows) against the page's
  * fused kernel (one CTA per row block walks all of K and keeps the running
  * total, so only the total is stored; the page's module docstring).  Their
  * statistics are bit-identical.

@@ -36,7 +36,7 @@ def f32_round_exact(q: Fraction) -> np.float32:
 # ---------------------------------------------------------------- exactness facts
 
 def test_bf16_values_are_exact_in_tf32():
-    """Page docstring, tf32x3 bullet: a bf16 value is exactly representable in tf32.
+    """Every bf16 value fits tf32 without rounding (page docstring, tf32x3 bullet).
 
     Round every finite bf16 to a 10-bit mantissa (round to nearest, ties away, as
     cvt.rna.tf32.f32 does) and check nothing changes.
