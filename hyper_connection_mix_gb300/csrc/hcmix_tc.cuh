@@ -19,9 +19,10 @@
 //   * a compute warpgroup (one thread per row) reads its row from shared
 //     memory, sums the squares with the page's tree, splits x into the limbs
 //     x0 (grid-aligned) and x1 = x - x0, and stores both into its TMEM A area;
-//   * warp 1 issues 8 MMAs of M=128, N=96, K=16 with A in TMEM and B in shared
-//     memory:  B rows [0 | w0 | w1 | w2] against x1, then [w0 | w1 | w2 | w3]
-//     against x0, accumulating into the warpgroup's TMEM D:
+//   * the warpgroup's MMA warp (warp 1 for warpgroup 0, the last warp for
+//     warpgroup 1) issues 8 MMAs of M=128, N=96, K=16 with A in TMEM and B in
+//     shared memory:  B rows [0 | w0 | w1 | w2] against x1, then
+//     [w0 | w1 | w2 | w3] against x0, accumulating into the warpgroup's TMEM D:
 //       D = [x0.w0 | x0.w1 + x1.w0 | x0.w2 + x1.w1 | x0.w3 + x1.w2]
 //     (the first 24 columns are exact; x1.w3 ~ 2^-34 relative is dropped);
 //     the whole warp runs the issue loop and one elected lane issues a
@@ -63,8 +64,11 @@ constexpr int kWG = 2;
 // limbs of a slice (one B buffer per chunk) stay in shared memory across
 // them; each warpgroup has its own set, reloaded when its slice changes.
 constexpr int kBStages = kWG * kChunksPerSlice;
-constexpr int kFirstComputeWarp = 3;  // warp 0: x loads, 1: MMA, 2: W loads
-constexpr int kWarps = kFirstComputeWarp + 4 * kWG;
+constexpr int kFirstComputeWarp = 3;  // warp 0: x loads, 1: MMAs of warpgroup 0, 2: W loads
+// one MMA-issuing warp per warpgroup: warp 1 for warpgroup 0, the last warp
+// for warpgroup 1
+constexpr int kWarps = kFirstComputeWarp + 4 * kWG + 1;
+constexpr int kMmaWarp1 = kWarps - 1;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileM = 128;
 constexpr uint32_t kRowBytes = 128;                       // 64 bf16 per smem row
@@ -88,7 +92,7 @@ struct Bookkeeping {
   uint64_t empty_b[kBStages];
   uint64_t a_ready[kWG];
   uint64_t d_ready[kWG];
-  uint64_t drain;
+  uint64_t drain[kWG];
   uint32_t tmem_base;
   int abort;
   int never;  // stays 0: the abort flag of waits that must not be cut short
@@ -460,7 +464,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       mbar_init(smem_u32(&bk.a_ready[g]), kWarpArrivals);
       mbar_init(smem_u32(&bk.d_ready[g]), 1);
     }
-    mbar_init(smem_u32(&bk.drain), 1);
+    for (int g = 0; g < kWG; ++g) mbar_init(smem_u32(&bk.drain[g]), 1);
     bk.abort = 0;
     bk.never = 0;
     fence_mbarrier_init();
@@ -594,17 +598,23 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
             mbar_wait(smem_u32(&bk.full_b[g * kChunksPerSlice + c]), (uint32_t)(loads[g] - 1) & 1u,
                       never, kDrainLimitNs);
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer, chunks in sequence order (round, chunk,
-    // warpgroup).  Chunk i needs its warpgroup's x limbs (a_ready) and the W
-    // limb tile of its slice (full_b, phase = the warpgroup's slice count).
-    // In order, each wait depends only on earlier chunks, so no wait can close
-    // a cycle.  The whole warp runs the loop, the waits are warp votes and one
+  } else if (warp == 1 || warp == kMmaWarp1) {
+    // ---------------- MMA issuer of warpgroup gm, its chunks in sequence
+    // order (round, chunk).  One issuer per warpgroup: an issuing thread
+    // spends ~45 cycles per MMA and, once MMAs are queued, a few hundred
+    // cycles in any shared-memory access (its mbarrier waits included), so a
+    // single issuer for both warpgroups left the tensor pipe idle between
+    // chunks.  Each commit tracks the MMAs of the thread that issues it, so
+    // the two issuers' commits are independent.  Chunk i needs its
+    // warpgroup's x limbs (a_ready) and the W limb tile of its slice (full_b,
+    // phase = the warpgroup's slice count).  In order, each wait depends only
+    // on earlier chunks, so no wait can close a cycle.  The whole warp runs the loop, the waits are warp votes and one
     // elected lane issues each MMA and commit: a loop whose control flow the
     // compiler cannot prove warp-uniform issued MMAs at about half the rate.
     // per warpgroup: slice of its current unit, B loads so far, and whether
     // this round's unit is the last of its slice (tracked incrementally: the
     // units of a round are consecutive)
+    const int gm = warp == 1 ? 0 : 1;
     int64_t u_tile = u_begin % n_tiles, u_slice = u_begin / n_tiles;  // of unit u_begin + kWG * r
     int loads[kWG] = {0, 0}, cur[kWG] = {-1, -1};
     bool ok = true;
@@ -638,7 +648,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       for (int c = 0; ok && c < kChunksPerSlice; ++c) {
 #pragma unroll
         for (int g = 0; g < kWG; ++g) {
-          if (!ok || g >= act) continue;
+          if (!ok || g >= act || g != gm) continue;
           const int j = g * kChunksPerSlice + c;
           const uint32_t aph = (uint32_t)(r * kChunksPerSlice + c) & 1u;
           // the W buffer is waited for at its first use in a slice only
@@ -661,8 +671,8 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       }
     }
     if (!ok && lane == 0) fail(bk, err);
-    umma_commit_warp(smem_u32(&bk.drain));
-    mbar_wait(smem_u32(&bk.drain), 0, never, kDrainLimitNs);
+    umma_commit_warp(smem_u32(&bk.drain[gm]));
+    mbar_wait(smem_u32(&bk.drain[gm]), 0, never, kDrainLimitNs);
   } else {
     // ---------------- compute warpgroups: one thread per tile row
     const int g = (warp - kFirstComputeWarp) >> 2;
