@@ -7,8 +7,9 @@ fp32, hc_scale[3], hc_base[24], sinkhorn_iters 20 -> pre, post, comb.  Inputs
 are the seeded synthetic tensors of hcmix_inputs.
 
 Our arm prints one JSON line with:
-  value      device-timed us per call (CUDA events around K replays of a CUDA
-             graph holding one call; with N ranks, max elapsed / (K * N));
+  value      device-timed us per call (CUDA events around exactly K calls,
+             replayed from CUDA graphs of 10 calls and one remainder graph;
+             with N ranks, max elapsed / (K * N));
   roofline   the contraction kernel timed alone with CUDA events on its stream,
              algorithmic bytes (x once + W once) / average duration, against the
              measured HBM copy bandwidth;
@@ -24,6 +25,9 @@ sweep M in {1, 4, 16, 64, 128, 256} on both paths, M = 512 with outlier
 channels, the stock split-K / fused full-K A/B at M in {512, 1024, 2048, 4096},
 the 4096-row call on a W packed once, and one 86-call forward (M = 16384, distinct W / scale / base per
 call) replayed from a single CUDA graph.
+`--protocols` times the 4096-row call with four x buffers in rotation and with
+a 512 MB L2 scrub before each call, and the oracle on one thread and on every
+host core for the 16-, 512-, 4096-row, decode and 86-call configurations.
 Multi-GPU (torchrun): each rank runs its own 4096 rows (weak scaling, rows are
 independent, no collective on the data path).
 """
@@ -66,6 +70,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="time the other workloads (one JSON line each) instead of the headline")
+    ap.add_argument("--protocols", action="store_true",
+                    help="the 4096-row call with rotated x buffers and with a scrubbed L2, and "
+                         "the oracle on one thread and on every host core (one JSON line each)")
     return ap.parse_args(argv)
 
 
@@ -274,24 +281,21 @@ def run_ours(args, rank, world, local):
     with torch.cuda.stream(stream):
         call()
         torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            call()
+        graphs = calls_graphs(call, stream)
     launches_per_call = 2 if path == "simt" else 3
 
-    # ---- device-timed value: K graph replays
+    # ---- device-timed value: exactly K calls, as CUDA-graph replays of
+    # GRAPH_CALLS calls each (and one remainder graph)
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
-            for _ in range(args.warmup):
-                graph.replay()
+            replay_calls(graphs, args.warmup)
         torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         with torch.cuda.stream(stream):
-            for _ in range(args.steps):
-                graph.replay()
+            replay_calls(graphs, args.steps)
         e1.record(stream)
         e1.synchronize()
         barrier(world)
@@ -302,21 +306,18 @@ def run_ours(args, rank, world, local):
     alg_bytes = traffic.algorithmic_bytes(M, K)
 
     # ---- dominant kernels alone: the contraction (W-limb pack + contraction),
-    # replayed from a CUDA graph so that host launch cost is not timed
+    # replayed from CUDA graphs so that host launch cost is not timed
     n_k = max(3, min(args.steps, 2000))
     with torch.cuda.stream(stream):
-        binding.hc_mix_contract(x, W, ws, stream=stream, path=path)
+        contract = lambda: binding.hc_mix_contract(x, W, ws, stream=stream, path=path)
+        contract()
         torch.cuda.synchronize()
-        kgraph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(kgraph, stream=stream):
-            binding.hc_mix_contract(x, W, ws, stream=stream, path=path)
-        for _ in range(3):
-            kgraph.replay()
+        kgraphs = calls_graphs(contract, stream)
+        replay_calls(kgraphs, 3 * GRAPH_CALLS)
         torch.cuda.synchronize()
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         c0.record(stream)
-        for _ in range(n_k):
-            kgraph.replay()
+        replay_calls(kgraphs, n_k)
         c1.record(stream)
         c1.synchronize()
     k_us = c0.elapsed_time(c1) * 1e3 / n_k
@@ -401,7 +402,8 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": M, "K": K, "path": path, "cuda_graph": True,
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "path": path,
+                   "cuda_graph": f"{GRAPH_CALLS} calls per graph replay",
                    "l2": "inputs larger than L2: x is 168 MB per call (L2 129 MB), no flush",
                    "inputs": "x bf16 N(0,1) seed 0 (rank r: rows 4096r..), W fp32 std K^-1/2"},
         "hbm_gbs": alg_bytes / (us_call * 1e-6) / 1e9,
@@ -422,6 +424,32 @@ def run_ours(args, rank, world, local):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+GRAPH_CALLS = 10  # calls per CUDA graph in the timed loops
+
+
+def calls_graphs(fn, stream):
+    """CUDA graphs holding GRAPH_CALLS calls of fn() and one call of it."""
+    import torch
+    graphs = []
+    for n in (GRAPH_CALLS, 1):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                fn()
+        graphs.append(g)
+    return graphs
+
+
+def replay_calls(graphs, calls: int) -> None:
+    """Exactly `calls` calls: replays of the GRAPH_CALLS-call graph, then of
+    the one-call graph for the remainder."""
+    many, one = graphs
+    for _ in range(calls // GRAPH_CALLS):
+        many.replay()
+    for _ in range(calls % GRAPH_CALLS):
+        one.replay()
 
 
 def graph_us(fn, stream, replays: int, warmup: int = 5) -> float:
@@ -552,6 +580,97 @@ def run_sweep(args):
                       "roofline_us_at_8tbs": calls * per_call / 8e12 * 1e6}), flush=True)
 
 
+def run_protocols(args):
+    """The 4096-row call timed two more ways, and the oracle's timings.
+
+    GPU: (i) four distinct x buffers in rotation, one CUDA graph of four calls
+    (x never comes from L2; W stays warm); (ii) each call alone after a 512 MB
+    memset that is not timed (x and W cold), median of the calls.  Host: the
+    oracle on one thread and on every host core for the 16-row, 512-row
+    (outlier), 4096-row and decode configurations in full, and for the 86-call
+    forward at 16384 rows on every core (the one-thread figure is one call,
+    scaled by 86, and says so)."""
+    import numpy as np
+    import torch
+
+    import hcmix_inputs as hi
+    import oracle
+    from hyper_connection_mix_gb300 import binding, traffic
+
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device)
+    M, K = M_ROWS, K_COLS
+    dev = lambda a: torch.from_numpy(a).to(device)
+    x_h = hi.make_x(M)
+    W_h, sc_h, bs_h = hi.make_w(), hi.make_scale(), hi.make_base()
+    W, sc, bs = dev(W_h), dev(sc_h), dev(bs_h)
+    xs = [torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).to(device) for _ in range(4)]
+    ws = binding.alloc_workspace(M, K, device)
+    out = (torch.empty(M, 4, device=device), torch.empty(M, 4, device=device),
+           torch.empty(M, 4, 4, device=device))
+    alg = traffic.algorithmic_bytes(M, K)
+
+    def call(x):
+        binding.hc_mix_fused(x, W, sc, bs, ITERS, RMS_EPS, HC_EPS, out=out, workspace=ws,
+                             stream=stream, path="auto")
+
+    def rotation():
+        for x in xs:
+            call(x)
+    us = graph_us(rotation, stream, replays=max(3, min(args.steps, 200)), warmup=args.warmup) / 4
+    print(json.dumps({"config": f"M={M} K={K}, 4 x buffers in rotation (warm W)",
+                      "us_per_call": us, "hbm_gbs": alg / (us * 1e-6) / 1e9}), flush=True)
+
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    times = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + max(3, min(args.steps, 100))):
+            scrub.fill_(i & 0xff)
+            e0.record(stream)
+            call(xs[0])
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1) * 1e3)
+    us = float(np.median(times))
+    print(json.dumps({"config": f"M={M} K={K}, each call after a 512 MB scrub (cold x and W)",
+                      "us_per_call": us, "hbm_gbs": alg / (us * 1e-6) / 1e9,
+                      "calls": len(times)}), flush=True)
+    del xs, scrub
+    torch.cuda.empty_cache()
+
+    # the oracle: one thread and every core, in full
+    oracle.build()
+    cores = host_cores()
+
+    def oracle_s(x, W_, sc_, bs_, threads):
+        t0 = time.perf_counter()
+        oracle.fused(np.ascontiguousarray(x), W_, sc_, bs_, ITERS, RMS_EPS, HC_EPS, threads=threads)
+        return time.perf_counter() - t0
+    cases = [("M=16", x_h[:16]), ("M=512 outliers", hi.make_x(512, outliers=True)),
+             (f"M={M}", x_h)] + [(f"decode M={m}", x_h[:m]) for m in (1, 4, 16, 64, 128, 256)]
+    for name, x in cases:
+        for threads in (1, cores):
+            s_ = oracle_s(x, W_h, sc_h, bs_h, threads)
+            print(json.dumps({"config": f"oracle {name} K={K}", "threads": threads,
+                              "us_per_call": s_ * 1e6}), flush=True)
+    M5, calls = 16384, 86
+    x5 = hi.make_x(M5)
+    t_all = 0.0
+    for i in range(calls):
+        s_w, s_s, s_b = hi.layer_seeds(i)
+        t_all += oracle_s(x5, hi.make_w(seed=s_w), hi.make_scale(seed=s_s),
+                          hi.make_base(seed=s_b), cores)
+    s_w, s_s, s_b = hi.layer_seeds(0)
+    t_one = oracle_s(x5, hi.make_w(seed=s_w), hi.make_scale(seed=s_s), hi.make_base(seed=s_b), 1)
+    print(json.dumps({"config": f"oracle 86-call forward M={M5} K={K}", "threads": cores,
+                      "us_per_forward": t_all * 1e6}), flush=True)
+    print(json.dumps({"config": f"oracle 86-call forward M={M5} K={K}", "threads": 1,
+                      "us_per_forward": t_one * calls * 1e6,
+                      "extrapolated": "one call on one thread, times 86"}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.warmup < 3:
@@ -560,6 +679,10 @@ def main(argv=None):
     if args.sweep:
         if rank == 0:
             run_sweep(args)
+        return
+    if args.protocols:
+        if rank == 0:
+            run_protocols(args)
         return
     if args.impl == "reference":
         run_reference(args, rank, world)
