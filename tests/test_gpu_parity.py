@@ -209,6 +209,28 @@ def test_device_status_clean_after_runs(path):
     assert binding.hc_mix_device_status(ws) == 0
 
 
+def test_small_batches_reuse_one_workspace(path):
+    """Decode-sized calls that share one workspace give the oracle's results
+    every time, with and without the statistics, and leave no device error."""
+    K = 2048
+    W, sc, bs = hi.make_w(K=K), hi.make_scale(), hi.make_base()
+    for M in (1, 5, 16):
+        x = hi.make_x(M, K=K)
+        want = oracle.fused(x, W, sc, bs, threads=THREADS)
+        xt, Wt, sct, bst = dev_x(x), dev(W), dev(sc), dev(bs)
+        ws = binding.alloc_workspace(M, K)
+        for rep in range(4):
+            out = binding.hc_mix_fused(xt, Wt, sct, bst, want_stats=rep % 2 == 1, workspace=ws,
+                                       path=path)
+            torch.cuda.synchronize()
+            got = [o.cpu().numpy() for o in out]
+            assert_epilogue_close(got[:3], want[:3], f"M={M} call {rep}")
+            if rep % 2 == 1:
+                assert_mix_close(got[3], want[3], f"M={M} call {rep}")
+                assert np.array_equal(got[4], want[4]), f"M={M} call {rep}: sq"
+        assert binding.hc_mix_device_status(ws) == 0
+
+
 def test_paths_agree_on_overlapping_sizes():
     if not (path_available("simt") and path_available("tc")):
         pytest.fail("both kernel paths must be available")
