@@ -416,7 +416,11 @@ def run_ours(args, rank, world, local):
                      "algorithmic_bytes": alg_bytes},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "calls_per_step": n_blocks, "rows_per_call": rows_b,
+                "note": (f"one step = {n_blocks} hc_mix_fused calls of {rows_b} rows each "
+                         f"(each converts W again), every call starting once its rows "
+                         f"have landed from pinned host memory")},
         "gpu_launches": args.steps * launches_per_call,
         "clocks": clk.summary(),
     }

@@ -192,7 +192,11 @@ hcmix_path hc_mix_auto_path(int64_t M);
  *     HCMIX_ERR_WORKSPACE before anything is launched.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address once and keeps it for later calls; make that
- *     first call before any stream capture starts on that device.
+ *     first call before any stream capture starts on that device.  The kept
+ *     address belongs to the device's current context: after a context reset
+ *     (cudaDeviceReset, or a primary context released and created again) it no
+ *     longer points at the array, so do not call this entry point again in a
+ *     process that has reset the device.
  *   - All calls share the one array, which keeps the last call's contents.
  *     Every call writes all the scratch it reads, so nothing needs clearing,
  *     but calls whose kernels overlap on the GPU (different streams, or

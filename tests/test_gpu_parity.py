@@ -13,6 +13,7 @@ import torch
 import hcmix_inputs as hi
 import oracle
 from hyper_connection_mix_gb300 import binding
+from pin_inputs import rms_pin_closed_form, rms_pin_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -113,6 +114,23 @@ def test_config_m4096_full(path):
     ratio = check_all(hi.make_x(4096), hi.make_w(), hi.make_scale(), hi.make_base(), path,
                       "M=4096")
     print(f"M=4096 {path}: max mix error / tolerance = {ratio:.3f}")
+
+
+@pytest.mark.parametrize("case", ["one_hot", "all_ones"])
+def test_rms_eps_placement_inputs(path, case):
+    """Inputs on which r = 1/sqrt(sq/K + rms_eps) is an exact power of two with
+    sq/K and rms_eps of one size: the kernels agree with the oracle and with
+    the closed form, which a misplaced eps or a dropped 1/K would miss by far."""
+    x, W, eps, r, c = rms_pin_inputs(case)
+    scale = np.array([1.0, 2.0, 3.0], np.float32)
+    base = (np.arange(24) * 0.03 - 0.2).astype(np.float32)
+    check_all(x, W, scale, base, path, f"rms {case}", rms_eps=eps)
+    got = run(x, W, scale, base, path, rms_eps=eps)
+    assert np.array_equal(got[3][0].astype(np.float64) * r, c)
+    p, q, C = rms_pin_closed_form(c, scale, base)
+    assert np.max(np.abs(got[0][0] - p)) <= 1e-6
+    assert np.max(np.abs(got[1][0] - q)) <= 1e-6
+    assert np.max(np.abs(got[2][0] - C)) <= 1e-5
 
 
 def test_integer_inputs_bit_exact(path):

@@ -12,6 +12,7 @@ import pytest
 
 import hcmix_inputs as hi
 import oracle
+from pin_inputs import rms_pin_closed_form, rms_pin_inputs
 
 F32 = np.float32
 TWO24 = 2.0 ** 24
@@ -362,3 +363,29 @@ def test_sinkhorn_rows_converge_on_moderate_logits():
         C = oracle.sinkhorn(np.exp(rng.uniform(-1, 1, (4, 4))).astype(np.float32), 20)
         np.testing.assert_allclose(C.sum(1), 1.0, atol=1e-5)
         np.testing.assert_allclose(C.sum(0), 1.0, atol=4 * 2 ** -23)
+
+
+# ---------------------------------------------------------------- rms placement
+
+@pytest.mark.parametrize("case", ["one_hot", "all_ones"])
+def test_rms_eps_inside_the_root_and_one_over_k(case):
+    """r = 1/sqrt(sq * (1/K) + rms_eps): on these inputs r is exact, so the
+    oracle's logits equal the closed form to rounding, and each plausible
+    misreading (eps outside the root, eps after the reciprocal, no 1/K) moves
+    mix * r, hence the outputs, far outside the epilogue tolerance."""
+    x, W, eps, r, c = rms_pin_inputs(case)
+    K = x.shape[1]
+    scale = np.array([1.0, 2.0, 3.0], np.float32)
+    base = (np.arange(24) * 0.03 - 0.2).astype(np.float32)
+    pre, post, comb, mix, sq = oracle.fused(x, W, scale, base, iters=20, rms_eps=eps)
+    assert np.array_equal(mix[0].astype(np.float64) * r, c)
+    p, q, C = rms_pin_closed_form(c, scale, base)
+    np.testing.assert_allclose(pre[0], p, atol=3e-7)
+    np.testing.assert_allclose(post[0], q, atol=5e-7)
+    np.testing.assert_allclose(comb[0], C, atol=2e-6)
+    s = float(sq[0]) / K
+    mix64 = mix[0].astype(np.float64)
+    for wrong_r in (1 / (np.sqrt(s) + eps), 1 / np.sqrt(s) + eps, 1 / np.sqrt(float(sq[0]) + eps)):
+        pw, qw, Cw = rms_pin_closed_form(mix64 * wrong_r, scale, base)
+        worst = max(np.abs(pw - p).max(), np.abs(qw - q).max(), np.abs(Cw - C).max())
+        assert worst > 1e-3, f"misreading r = {wrong_r} would go unnoticed"
