@@ -23,7 +23,7 @@ HC = 4
 STATUS = {0: "HCMIX_OK", 1: "HCMIX_ERR_INVALID_ARG", 2: "HCMIX_ERR_ALIGNMENT",
           3: "HCMIX_ERR_UNSUPPORTED", 4: "HCMIX_ERR_WORKSPACE", 5: "HCMIX_ERR_CUDA",
           6: "HCMIX_ERR_DEVICE"}
-PATHS = {"auto": 0, "simt": 1, "tc": 2, "simt_fullk": 3, "tc_tf32x3": 4}
+PATHS = {"auto": 0, "simt": 1, "tc": 2, "simt_fullk": 3, "tc_tf32x3": 4, "tc_staged": 5}
 
 # every symbol include/hcmix.h declares
 EXPORTS = ("hc_mix_workspace_bytes", "hc_mix_stats", "hc_mix_sinkhorn", "hc_mix_fused",

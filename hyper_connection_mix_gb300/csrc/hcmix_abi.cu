@@ -36,10 +36,8 @@ constexpr int64_t kReduceSmallMaxM = 16;
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Workspace {
-  size_t err_off = 0;     // uint32 device error word (256-byte header)
-  size_t limbs_off = 0;   // packed W for the tensor-core path: bf16 limbs [4][24][K]
-                          // (exact) or fp32 tf32x3 parts [2][24][K], the same size
-  size_t limbs_bytes = 0;
+  size_t err_off = 0;     // 256-byte header: device error word at byte 0, the tensor-core
+                          // kernel's grid-barrier count at byte 64 and generation at byte 128
   size_t part_off = 0;    // fp32 partials [slices][25][Mpad]
   size_t part_bytes = 0;
   size_t total = 0;
@@ -52,9 +50,7 @@ Workspace workspace_layout(int64_t M, int64_t K) {
   w.n_slices = K / kSlice;
   w.Mpad = (M + 127) / 128 * 128;
   w.err_off = 0;
-  w.limbs_off = kAlign;
-  w.limbs_bytes = align_up((size_t)4 * kMix * (size_t)K * 2, kAlign);
-  w.part_off = w.limbs_off + w.limbs_bytes;
+  w.part_off = kAlign;
   w.part_bytes = align_up((size_t)w.n_slices * kPartStride * (size_t)w.Mpad * 4, kAlign);
   w.total = w.part_off + w.part_bytes;
   return w;
@@ -114,7 +110,8 @@ hcmix_status simt_smem_attributes() {
 
 bool valid_path(hcmix_path path) {
   return path == HCMIX_PATH_AUTO || path == HCMIX_PATH_SIMT || path == HCMIX_PATH_TC ||
-         path == HCMIX_PATH_SIMT_FULLK || path == HCMIX_PATH_TC_TF32X3;
+         path == HCMIX_PATH_SIMT_FULLK || path == HCMIX_PATH_TC_TF32X3 ||
+         path == HCMIX_PATH_TC_STAGED;
 }
 
 hcmix_path resolve_path(hcmix_path path, int64_t M) {
@@ -122,14 +119,15 @@ hcmix_path resolve_path(hcmix_path path, int64_t M) {
   return path;
 }
 
-// Contraction into the workspace partials (one launch or two).
-hcmix_status launch_contraction(const void* x, int64_t x_stride, const float* W,
-                                int64_t w_stride, int64_t M, int64_t K, void* workspace,
-                                cudaStream_t stream, hcmix_path path) {
+bool is_tc(hcmix_path path) { return path == HCMIX_PATH_TC || path == HCMIX_PATH_TC_TF32X3; }
+
+// CUDA-core contraction into the workspace partials (one launch).
+hcmix_status launch_simt_contraction(const void* x, int64_t x_stride, const float* W,
+                                     int64_t w_stride, int64_t M, int64_t K, void* workspace,
+                                     cudaStream_t stream, hcmix_path path) {
   const Workspace ws = workspace_layout(M, K);
   char* base = static_cast<char*>(workspace);
   float* part = reinterpret_cast<float*>(base + ws.part_off);
-  path = resolve_path(path, M);
   if (path == HCMIX_PATH_SIMT) {
     dim3 grid((unsigned)((M + kSimtRows - 1) / kSimtRows), (unsigned)ws.n_slices);
     if (simt_smem_attributes() != HCMIX_OK) return HCMIX_ERR_CUDA;
@@ -144,24 +142,17 @@ hcmix_status launch_contraction(const void* x, int64_t x_stride, const float* W,
                                         (int)M, (int)ws.Mpad, (int)ws.n_slices, part);
     return launch_status();
   }
-  if (path == HCMIX_PATH_TC || path == HCMIX_PATH_TC_TF32X3) {
-    return tc_launch(static_cast<const uint16_t*>(x), x_stride, W, w_stride, M, K,
-                     base + ws.limbs_off, part, (int)ws.Mpad,
-                     reinterpret_cast<uint32_t*>(base + ws.err_off), stream,
-                     path == HCMIX_PATH_TC_TF32X3);
-  }
   return HCMIX_ERR_INVALID_ARG;
 }
 
 // Ordered reduce of the stored slices (the full-K kernel stores one) and,
-// with do_epilogue, the epilogue.
+// with do_epilogue, the epilogue: the CUDA-core paths' second launch.
 hcmix_status launch_reduce(int64_t M, int64_t K, void* workspace, const float* hc_scale,
                            const float* hc_base, int iters, float rms_eps, float hc_eps,
                            float* pre, float* post, float* comb, float* mix_out, float* sq_out,
                            int do_epilogue, cudaStream_t stream, hcmix_path path) {
   const Workspace ws = workspace_layout(M, K);
-  const int stored_slices =
-      resolve_path(path, M) == HCMIX_PATH_SIMT_FULLK ? 1 : (int)ws.n_slices;
+  const int stored_slices = path == HCMIX_PATH_SIMT_FULLK ? 1 : (int)ws.n_slices;
   const float* part =
       reinterpret_cast<const float*>(static_cast<const char*>(workspace) + ws.part_off);
   const float inv_k = (float)(1.0 / (double)K);
@@ -177,6 +168,32 @@ hcmix_status launch_reduce(int64_t M, int64_t K, void* workspace, const float* h
       part, stored_slices, (int)ws.Mpad, (int)M, inv_k, hc_scale, hc_base, iters, rms_eps,
       hc_eps, pre, post, comb, mix_out, sq_out, do_epilogue);
   return launch_status();
+}
+
+// One call on `path`: tail 0 = contraction only (partials), 1 = + mix / sq,
+// 2 = + epilogue.  The tensor-core paths run everything in one launch; the
+// CUDA-core paths run the contraction and then the reduce kernel.  W null
+// with `packed` set: the tensor-core path on limbs packed ahead of time.
+hcmix_status run_path(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
+                      const void* packed, int64_t M, int64_t K, void* workspace, int tail,
+                      const float* hc_scale, const float* hc_base, int iters, float rms_eps,
+                      float hc_eps, float* pre, float* post, float* comb, float* mix_out,
+                      float* sq_out, cudaStream_t stream, hcmix_path path) {
+  path = resolve_path(path, M);
+  const Workspace ws = workspace_layout(M, K);
+  char* base = static_cast<char*>(workspace);
+  if (is_tc(path) || path == HCMIX_PATH_TC_STAGED) {
+    TcTail t = {tail, (float)(1.0 / (double)K), hc_scale, hc_base, iters, rms_eps, hc_eps, pre,
+                post, comb, mix_out, sq_out};
+    return tc_launch(static_cast<const uint16_t*>(x), x_stride, W, w_stride, M, K, packed,
+                     reinterpret_cast<float*>(base + ws.part_off), (int)ws.Mpad,
+                     reinterpret_cast<uint32_t*>(base + ws.err_off), t, stream,
+                     path == HCMIX_PATH_TC_TF32X3, path == HCMIX_PATH_TC_STAGED);
+  }
+  hcmix_status st = launch_simt_contraction(x, x_stride, W, w_stride, M, K, workspace, stream, path);
+  if (st != HCMIX_OK || tail == 0) return st;
+  return launch_reduce(M, K, workspace, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post,
+                       comb, mix_out, sq_out, tail == 2 ? 1 : 0, stream, path);
 }
 
 }  // namespace
@@ -203,11 +220,9 @@ hcmix_status hc_mix_stats_ex(const void* x, int64_t x_stride, const float* W, in
   if (!valid_path(path)) return HCMIX_ERR_INVALID_ARG;
   if (M == 0) return HCMIX_OK;
   if (mix_out == nullptr || sq_out == nullptr) return HCMIX_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = launch_contraction(x, x_stride, W, w_stride, M, K, workspace, s, path);
-  if (st != HCMIX_OK) return st;
-  return launch_reduce(M, K, workspace, nullptr, nullptr, 0, 0.f, 0.f, nullptr, nullptr, nullptr,
-                       mix_out, sq_out, 0, s, path);
+  return run_path(x, x_stride, W, w_stride, nullptr, M, K, workspace, 1, nullptr, nullptr, 0,
+                  0.f, 0.f, nullptr, nullptr, nullptr, mix_out, sq_out,
+                  static_cast<cudaStream_t>(stream), path);
 }
 
 hcmix_status hc_mix_contract_ex(const void* x, int64_t x_stride, const float* W,
@@ -219,8 +234,9 @@ hcmix_status hc_mix_contract_ex(const void* x, int64_t x_stride, const float* W,
   if (st != HCMIX_OK) return st;
   if (!valid_path(path)) return HCMIX_ERR_INVALID_ARG;
   if (M == 0) return HCMIX_OK;
-  return launch_contraction(x, x_stride, W, w_stride, M, K, workspace,
-                            static_cast<cudaStream_t>(stream), path);
+  return run_path(x, x_stride, W, w_stride, nullptr, M, K, workspace, 0, nullptr, nullptr, 0,
+                  0.f, 0.f, nullptr, nullptr, nullptr, nullptr, nullptr,
+                  static_cast<cudaStream_t>(stream), path);
 }
 
 hcmix_status hc_mix_stats(const void* x, int64_t x_stride, const float* W, int64_t w_stride,
@@ -262,11 +278,9 @@ hcmix_status hc_mix_fused_ex(const void* x, int64_t x_stride, const float* W, in
   if (st != HCMIX_OK) return st;
   if (!valid_path(path)) return HCMIX_ERR_INVALID_ARG;
   if (M == 0) return HCMIX_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = launch_contraction(x, x_stride, W, w_stride, M, K, workspace, s, path);
-  if (st != HCMIX_OK) return st;
-  return launch_reduce(M, K, workspace, hc_scale, hc_base, sinkhorn_iters, rms_eps, hc_eps, pre,
-                       post, comb, mix_out, sq_out, 1, s, path);
+  return run_path(x, x_stride, W, w_stride, nullptr, M, K, workspace, 2, hc_scale, hc_base,
+                  sinkhorn_iters, rms_eps, hc_eps, pre, post, comb, mix_out, sq_out,
+                  static_cast<cudaStream_t>(stream), path);
 }
 
 size_t hc_mix_packed_w_bytes(int64_t K, int mix) {
@@ -305,15 +319,9 @@ hcmix_status hc_mix_fused_packed(const void* x, int64_t x_stride, const void* pa
   if (packed_bytes < hc_mix_packed_w_bytes(K, mix) ||
       workspace_bytes < workspace_layout(M, K).total)
     return HCMIX_ERR_WORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Workspace ws = workspace_layout(M, K);
-  char* base = static_cast<char*>(workspace);
-  st = tc_launch(static_cast<const uint16_t*>(x), x_stride, nullptr, 0, M, K,
-                 const_cast<void*>(packed_w), reinterpret_cast<float*>(base + ws.part_off),
-                 (int)ws.Mpad, reinterpret_cast<uint32_t*>(base + ws.err_off), s, false);
-  if (st != HCMIX_OK) return st;
-  return launch_reduce(M, K, workspace, hc_scale, hc_base, sinkhorn_iters, rms_eps, hc_eps, pre,
-                       post, comb, mix_out, sq_out, 1, s, HCMIX_PATH_TC);
+  return run_path(x, x_stride, nullptr, 0, packed_w, M, K, workspace, 2, hc_scale, hc_base,
+                  sinkhorn_iters, rms_eps, hc_eps, pre, post, comb, mix_out, sq_out,
+                  static_cast<cudaStream_t>(stream), HCMIX_PATH_TC);
 }
 
 hcmix_status hc_mix_fused(const void* x, int64_t x_stride, const float* W, int64_t w_stride,

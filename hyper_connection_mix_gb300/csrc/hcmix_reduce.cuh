@@ -9,7 +9,7 @@
 // lane), so every load of a (slice, j) pair is 32 consecutive floats.  Each
 // lane issues its slice loads in batches of 40 before adding them in slice
 // order, so the L2 latency is paid per batch rather than per slice.  The
-// first 512 threads then run the epilogue, 16 per row.
+// first 32 threads then run the epilogue, one row each.
 #pragma once
 
 #include "hcmix_common.cuh"
@@ -20,53 +20,94 @@ constexpr int kReduceRows = 32;
 constexpr int kReduceThreads = 32 * kPartStride;
 constexpr int kReduceBatch = 40;
 
-// Epilogue of the CTA's 32 rows from their totals in shared memory
-// (s_tot[j][r]: j < 24 mix, j = 24 sum of squares): 16 threads per row,
-// thread e owns comb entry e = 4i + j and, for e < 8, logit e of pre (e < 4)
-// or post.  Sinkhorn sums are gathered with shuffles and added in index
-// order, as one thread per row would.  The CTA's first nrows rows are done
-// (nrows <= 32 and nrows * 16 a multiple of 32, so that whole warps take
-// part in the shuffles); threads nrows * 16 and up do nothing.
-__device__ __forceinline__ void epilogue16(const float (&s_tot)[kPartStride][kReduceRows + 1],
-                                           int row0, int nrows, int M, float inv_k,
-                                           const float* __restrict__ hc_scale,
-                                           const float* __restrict__ hc_base, int iters,
-                                           float rms_eps, float hc_eps, float* __restrict__ pre,
-                                           float* __restrict__ post, float* __restrict__ comb) {
-  const int tid = threadIdx.x;
-  if (tid >= nrows * kHc * kHc) return;
-  const int rloc = tid >> 4, e = tid & 15;
-  const int row = row0 + rloc;
-  const int gbase = threadIdx.x & 16;  // first lane of this row's 16-lane group
-  const float sq = s_tot[kMix][rloc];
-  const float v = __fadd_rn(__fmul_rn(sq, inv_k), rms_eps);
+// 1 / s for a Sinkhorn normalisation, by which the row's (column's) four
+// entries are then multiplied: the fast approximate reciprocal (within 1 ulp;
+// with the product, each entry is within 2 ulp of c / s, and the iteration's
+// own contraction keeps the result within a few ulp of the correctly rounded
+// sequence), and the IEEE quotient when s is below the normal range, where
+// the fast form flushes to zero.
+__device__ __forceinline__ float sinkhorn_rcp(float s) {
+  if (s < 1.17549435e-38f) return __fdiv_rn(1.0f, s);
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+
+// The epilogue of one row, by one thread, from the row's totals (s_tot[j][r]:
+// j < 24 mix, j = 24 sum of squares): r = 1/sqrt(sq (1/K) + rms_eps); logit
+// j = mix_j r scale[g(j)] + base_j; pre = sigmoid, post = 2 sigmoid;
+// Sinkhorn on exp of the 16 comb logits, rows then columns, sums in index
+// order.  The row and column reciprocals of a normalisation are taken once
+// (sinkhorn_rcp) and multiplied in.  Rows at or past
+// row_end are not written.
+__device__ __forceinline__ void epilogue_row(const float (&s_tot)[kPartStride][kReduceRows + 1],
+                                             int r, int row, int row_end, float inv_k,
+                                             const float* __restrict__ hc_scale,
+                                             const float* __restrict__ hc_base, int iters,
+                                             float rms_eps, float hc_eps,
+                                             float* __restrict__ pre, float* __restrict__ post,
+                                             float* __restrict__ comb) {
+  const float v = __fadd_rn(__fmul_rn(s_tot[kMix][r], inv_k), rms_eps);
   const float rr = __fdiv_rn(1.0f, __fsqrt_rn(v));
-  if (e < 2 * kHc) {
+  float pp[2 * kHc];
+#pragma unroll
+  for (int e = 0; e < 2 * kHc; ++e) {
     const float sc = e < kHc ? hc_scale[0] : hc_scale[1];
-    const float lg = __fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][rloc], rr), sc), hc_base[e]);
-    const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lg)));
-    if (row < M) {
-      if (e < kHc) pre[(int64_t)row * kHc + e] = sg;
-      else post[(int64_t)row * kHc + (e - kHc)] = __fmul_rn(2.0f, sg);
+    const float lg = __fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][r], rr), sc), hc_base[e]);
+    pp[e] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lg)));
+  }
+  float c[kHc][kHc];
+#pragma unroll
+  for (int i = 0; i < kHc; ++i)
+#pragma unroll
+    for (int jj = 0; jj < kHc; ++jj) {
+      const int e = 2 * kHc + kHc * i + jj;
+      c[i][jj] = expf(__fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][r], rr), hc_scale[2]), hc_base[e]));
+    }
+  // every sum is of positive values, so s + 0 = s: the eps add is skipped at 0
+  const bool add_eps = hc_eps != 0.0f;
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < kHc; ++i) {
+      float s = __fadd_rn(__fadd_rn(__fadd_rn(c[i][0], c[i][1]), c[i][2]), c[i][3]);
+      if (add_eps) s = __fadd_rn(s, hc_eps);
+      const float rs = sinkhorn_rcp(s);
+#pragma unroll
+      for (int jj = 0; jj < kHc; ++jj) c[i][jj] = __fmul_rn(c[i][jj], rs);
+    }
+#pragma unroll
+    for (int jj = 0; jj < kHc; ++jj) {
+      float s = __fadd_rn(__fadd_rn(__fadd_rn(c[0][jj], c[1][jj]), c[2][jj]), c[3][jj]);
+      if (add_eps) s = __fadd_rn(s, hc_eps);
+      const float rs = sinkhorn_rcp(s);
+#pragma unroll
+      for (int i = 0; i < kHc; ++i) c[i][jj] = __fmul_rn(c[i][jj], rs);
     }
   }
-  const float lgc = __fadd_rn(__fmul_rn(__fmul_rn(s_tot[2 * kHc + e][rloc], rr), hc_scale[2]),
-                              hc_base[2 * kHc + e]);
-  float c = expf(lgc);
-  const int ci = e >> 2, cj = e & 3;
-  for (int it = 0; it < iters; ++it) {
-    float s = __shfl_sync(0xffffffffu, c, gbase + 4 * ci);
-    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 4 * ci + 1));
-    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 4 * ci + 2));
-    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 4 * ci + 3));
-    c = __fdiv_rn(c, __fadd_rn(s, hc_eps));
-    s = __shfl_sync(0xffffffffu, c, gbase + cj);
-    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 4 + cj));
-    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 8 + cj));
-    s = __fadd_rn(s, __shfl_sync(0xffffffffu, c, gbase + 12 + cj));
-    c = __fdiv_rn(c, __fadd_rn(s, hc_eps));
+  if (row >= row_end) return;
+#pragma unroll
+  for (int e = 0; e < kHc; ++e) {
+    pre[(int64_t)row * kHc + e] = pp[e];
+    post[(int64_t)row * kHc + e] = __fmul_rn(2.0f, pp[kHc + e]);
   }
-  if (row < M) comb[(int64_t)row * kHc * kHc + e] = c;
+#pragma unroll
+  for (int i = 0; i < kHc; ++i)
+#pragma unroll
+    for (int jj = 0; jj < kHc; ++jj) comb[(int64_t)row * kHc * kHc + kHc * i + jj] = c[i][jj];
+}
+
+// The epilogue of the CTA's first nrows (<= 32) rows: one thread per row.
+__device__ __forceinline__ void epilogue_rows(const float (&s_tot)[kPartStride][kReduceRows + 1],
+                                              int row0, int nrows, int row_end, float inv_k,
+                                              const float* __restrict__ hc_scale,
+                                              const float* __restrict__ hc_base, int iters,
+                                              float rms_eps, float hc_eps,
+                                              float* __restrict__ pre, float* __restrict__ post,
+                                              float* __restrict__ comb) {
+  const int t = threadIdx.x;
+  if (t < nrows)
+    epilogue_row(s_tot, t, row0 + t, row_end, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps,
+                 pre, post, comb);
 }
 
 __global__ void __launch_bounds__(kReduceThreads)
@@ -102,14 +143,15 @@ hcmix_reduce_kernel(const float* __restrict__ part, int n_slices, int Mpad, int 
   }
   if (sq_out != nullptr && tid < kReduceRows && row0 + tid < M) sq_out[row0 + tid] = s_tot[kMix][tid];
   if (!do_epilogue) return;
-  epilogue16(s_tot, row0, kReduceRows, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post, comb);
+  epilogue_rows(s_tot, row0, kReduceRows, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post,
+                comb);
 }
 
 // Small-M variant (decode batches): 2 rows per CTA and one warp per output j.
 // All 32 lanes fetch the (row, j) values of the slices they own (slice s to
 // lane s % 32), so every load of a CTA is in flight at once; the values are
 // parked in shared memory and lane r of the warp then adds row r's slices in
-// slice order from zero.  Then the same 16-threads-per-row epilogue.
+// slice order from zero.  Then the same one-thread-per-row epilogue.
 constexpr int kReduceSmallRows = 2;
 constexpr int kReduceSmallMaxSlices = 128;  // slices held in shared memory (K <= 32768)
 
@@ -152,14 +194,14 @@ hcmix_reduce_small_kernel(const float* __restrict__ part, int n_slices, int Mpad
   if (sq_out != nullptr && tid < kReduceSmallRows && row0 + tid < M)
     sq_out[row0 + tid] = s_tot[kMix][tid];
   if (!do_epilogue) return;
-  epilogue16(s_tot, row0, kReduceSmallRows, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps,
-             pre, post, comb);
+  epilogue_rows(s_tot, row0, kReduceSmallRows, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps,
+                pre, post, comb);
 }
 
 // The epilogue alone from caller-provided mix[M, 24] and sq[M]: 32 rows per
 // CTA staged in shared memory in the reduce kernel's layout, then the same
-// 16-threads-per-row epilogue.
-constexpr int kEpilogueThreads = kReduceRows * kHc * kHc;
+// one-thread-per-row epilogue.
+constexpr int kEpilogueThreads = kReduceRows;
 
 __global__ void __launch_bounds__(kEpilogueThreads)
 hcmix_epilogue_kernel(const float* __restrict__ mix, const float* __restrict__ sq, int M,
@@ -177,7 +219,8 @@ hcmix_epilogue_kernel(const float* __restrict__ mix, const float* __restrict__ s
   if (threadIdx.x < kReduceRows)
     s_tot[kMix][threadIdx.x] = (int)threadIdx.x < rows ? sq[row0 + threadIdx.x] : 0.0f;
   __syncthreads();
-  epilogue16(s_tot, row0, kReduceRows, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post, comb);
+  epilogue_rows(s_tot, row0, kReduceRows, M, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps, pre, post,
+                comb);
 }
 
 }  // namespace hcmix

@@ -13,9 +13,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The "memory" clobber keeps the read in program order with the memory
+// operations and barriers around it.
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
   return t;
 }
 
@@ -89,36 +91,52 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Potentially blocking test of phase `parity` of `bar`: the thread may sleep
-// until the phase completes or about kSuspendHintNs pass, so a waiting warp
-// leaves the issue slots of its SM sub-partition to the others.
-constexpr uint32_t kSuspendHintNs = 20000;
-
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits until phase `parity` of `bar` completes.  Gives up (returns false)
-// after `limit_ns` of wall clock or when *abort becomes non-zero.
+// after `limit_ns` of wall clock or when *abort becomes non-zero.  It polls
+// with short sleeps rather than suspending in try_wait: a thread suspended
+// there resumed some hundreds of nanoseconds after the phase completed, and
+// the hand-offs of the pipeline are shorter than that.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile int* abort, uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait_sleep(bar, parity)) return true;
-    if ((i & 15u) == 0) {
+    __nanosleep(32);
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
+}
+
+// ---------------------------------------------------------------- global memory
+
+// Load with acquire semantics at GPU scope (sees what another CTA released).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Atomic add at GPU scope with release semantics (this thread's earlier
+// writes, and those ordered before it by a CTA barrier, are visible to any
+// thread that observes the new value with acquire semantics).
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Reduction (no result) at GPU scope with release semantics.
+__device__ __forceinline__ void red_add_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Named barrier `id` (1..15) over `count` threads of whole warps.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
@@ -144,6 +162,17 @@ __device__ __forceinline__ void stg_f32_hint(float* p, float v, uint64_t policy)
 
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// global -> shared, completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
 }
 
 // 2-D tiled bulk tensor load global -> shared, completing on `bar`.

@@ -1,49 +1,58 @@
-// Tensor-core (tcgen05) contraction path for sm_103a.
+// Tensor-core (tcgen05) path for sm_103a: the whole hc_mix_fused call in one
+// persistent kernel.
 //
 // Work: the rows are cut into 128-row tiles and K into 256-column slices (the
 // hc_fused page's slice grid); a unit is one (tile, slice) pair, numbered
 // slice-major.  Each CTA of a grid of min(#SMs, #units) takes a contiguous
-// range of units, so its units mostly share one slice, and writes, for each
-// unit, the slice totals of its 128 rows (24 mix values and the sum of
-// squares) to the workspace partials; hcmix_reduce_kernel then adds the
-// slices in slice order.
+// range of units, so its units come from at most two consecutive slices at the
+// workload sizes (more only when K exceeds 152 slices), and the W operand of
+// those slices stays in shared memory for the whole range.
 //
-// Per 64-column chunk (see hcmix_common.cuh for the numerics):
-//   * warp 0 (one thread) loads x with TMA, two chunks of a tile (32 KB) per
-//     load, into a 3-stage ring; warp 2 (one thread) loads the four W limbs of
-//     a slice [96 rows x 64 per chunk] into the B buffers of a warpgroup when
-//     that warpgroup reaches a new slice (128-byte swizzle for both).  The
-//     limbs come from hcmix_pack_limbs_kernel, except when every CTA owns one
-//     unit (small batches): the CTA then splits its slice of W into the B
-//     buffers itself during set-up;
-//   * a compute warpgroup (one thread per row) reads its row from shared
-//     memory, sums the squares with the page's tree, splits x into the limbs
-//     x0 (grid-aligned) and x1 = x - x0, and stores both into its TMEM A area;
-//   * the warpgroup's MMA warp (warp 1 for warpgroup 0, the last warp for
-//     warpgroup 1) issues 8 MMAs of M=128, N=96, K=16 with A in TMEM and B in
-//     shared memory:  B rows [0 | w0 | w1 | w2] against x1, then
-//     [w0 | w1 | w2 | w3] against x0, accumulating into the warpgroup's TMEM D:
+// One CTA = 16 warps with fixed roles, each role a stage of a pipeline over
+// the CTA's 64-column chunks (k = 0, 1, ... in unit order, four per unit):
+//   * warp 0 (one lane) loads x with TMA, two chunks of a tile (32 KB, 128-byte
+//     swizzle) per load, into a 3-stage ring;
+//   * the eight transform warps (warps 4..11, two per TMEM lane quadrant;
+//     warp 4 + 4h + q takes the chunks k with k % 2 == h for tile rows 32q..)
+//     read their row of the chunk, sum its squares by the page's fixed tree,
+//     split x into the limbs x0 (grid-aligned) and x1 = x - x0, and store both
+//     into TMEM A buffer k % 4 (x as fp32 in tf32x3 mode); the chunk's sum of
+//     squares goes to a shared-memory slot beside it;
+//   * warp 1 issues the chunk's 8 MMAs (M=128, N=96, K=16, A in TMEM, B in
+//     shared memory) into TMEM D buffer k % 2:  B rows [0 | w0 | w1 | w2]
+//     against x1, then [w0 | w1 | w2 | w3] against x0, so that
 //       D = [x0.w0 | x0.w1 + x1.w0 | x0.w2 + x1.w1 | x0.w3 + x1.w2]
-//     (the first 24 columns are exact; x1.w3 ~ 2^-34 relative is dropped);
-//     the whole warp runs the issue loop and one elected lane issues a
-//     chunk's MMAs and commit from one inline-assembly block, which keeps the
-//     loop warp-uniform and the issuer's instruction count small;
-//   * the warpgroup reads D and forms the chunk dot fl32(top + rest).
-// Two warpgroups work on two units at a time.  Each is software-pipelined: it
-// transforms chunk k+1 into its second TMEM A buffer before it waits for the
-// MMAs of chunk k, so the MMA latency hides behind the next transform; D is
-// released together with A(k+1).  TMEM holds 2 x (2 x 64 A + 96 D) columns.
+//     (the first 24 columns exact; x1.w3 ~ 2^-34 relative is dropped);
+//   * the four accumulate warps (warps 12..15, one per quadrant) read D, form
+//     the chunk dot fl32(top + ((r1 + r2) + r3)), add it into the slice total
+//     (chunks in order, from zero), add the chunk's sum of squares likewise,
+//     and at the end of each unit store its 24 + 1 slice totals per row to the
+//     workspace partials;
+//   * the W operand: every CTA converts the fp32 W of its first two slices
+//     into the exact bf16 limbs (or the tf32x3 big / small parts) in shared
+//     memory during set-up, with all 512 threads (no separate pack kernel);
+//     warp 2 refills a slot when a CTA covers more slices, or TMA-loads limbs
+//     that hc_mix_pack_w wrote ahead of time.
+// A buffer k % 4 is handed back when the accumulate warps have read chunk k
+// (which is after its MMAs have completed), D buffer k % 2 likewise, so the
+// transform warps run up to three chunks ahead of the MMAs and the MMAs of
+// chunk k + 1 execute while chunk k is being read.
+//
+// Tail (same kernel): once every CTA has stored its partials (a grid-wide
+// barrier; the launch is cooperative, so every CTA is resident), CTA b adds
+// the slice totals of rows [b M / G, (b + 1) M / G) in slice order from zero
+// and, for hc_mix_fused, runs the epilogue (rms, logits, pre / post, Sinkhorn)
+// on them; hc_mix_stats writes mix / sq instead.
 //
 // tf32x3 mode (hcmix_tc_kernel<true>): the hc_fused page's own chunk
-// arithmetic instead of the exact limbs.  W is packed as big = W rounded to
+// arithmetic instead of the exact limbs.  W is split as big = W rounded to
 // tf32 (nearest, ties away: the page's _tf32_rna) and small = W - big; x
 // (exact in tf32) goes to TMEM as fp32; per chunk the MMA warp issues, in the
 // page's order, dot(x, small) from zero and then dot(x, big) on top of it:
-// 2 x 8 MMAs of M=128, N=32 (24 outputs + 8 zero rows), K=8, kind::tf32, and
-// D's first 24 columns are the chunk dot.  The rest of the pipeline (units,
-// stages, barriers, sum of squares, partials) is the same.  The tensor
-// core's own rounding inside each MMA decides the last bits of every chunk
-// dot, so this mode is not exact; the page gives no bound either.
+// 2 x 8 MMAs of M=128, N=32, K=8, kind::tf32.  D's first 24 columns are the
+// chunk dot (columns 24..31 come from B rows past the 24 outputs and are never
+// read).  The tensor core's own rounding inside each MMA decides the last bits
+// of every chunk dot, so this mode is not exact; the page gives no bound either.
 #pragma once
 
 #include <cuda.h>
@@ -52,83 +61,120 @@
 
 #include "hcmix.h"
 #include "hcmix_common.cuh"
+#include "hcmix_reduce.cuh"
 #include "hcmix_sm100.cuh"
 
 namespace hcmix {
 namespace tc {
 
-constexpr int kXStages = 3;                                 // x stages in flight
+constexpr int kXStages = 3;        // x stages in flight
 constexpr int kChunksPerStage = 2;  // an x stage holds two chunks of a tile (one 32 KB load)
-constexpr int kWG = 2;
-// Units run slice-major, so a CTA's units mostly share one slice and the W
-// limbs of a slice (one B buffer per chunk) stay in shared memory across
-// them; each warpgroup has its own set, reloaded when its slice changes.
-constexpr int kBStages = kWG * kChunksPerSlice;
-constexpr int kFirstComputeWarp = 3;  // warp 0: x loads, 1: MMAs of warpgroup 0, 2: W loads
-// one MMA-issuing warp per warpgroup: warp 1 for warpgroup 0, the last warp
-// for warpgroup 1
-constexpr int kWarps = kFirstComputeWarp + 4 * kWG + 1;
-constexpr int kMmaWarp1 = kWarps - 1;
+constexpr int kNumA = 2;   // TMEM A buffers: A buffer h belongs to transform half h (chunks k % 2 == h)
+constexpr int kNumD = 4;   // TMEM D buffers: D buffer g belongs to MMA issuer g (chunks k % 4 == g)
+constexpr int kNumSq = 8;  // sum-of-squares slots (shared memory)
+constexpr int kSlots = 2;  // W slots: a CTA's consecutive slices alternate between them
+constexpr int kWBufs = kSlots * kChunksPerSlice;
+constexpr int kWarps = 17;
 constexpr int kThreads = kWarps * 32;
+constexpr int kXWarp = 0, kMmaWarp0 = 1;
+constexpr int kNumMma = 4;  // MMA-issuing warps 1..4: chunk k (= chunk c of its unit) to warp 1 + c
+constexpr int kFirstTWarp = 5;   // transform warps 5..12
+constexpr int kNumTWarps = 8;
+constexpr int kFirstDWarp = 13;  // accumulate warps 13..16
 constexpr int kTileM = 128;
-constexpr uint32_t kRowBytes = 128;                       // 64 bf16 per smem row
-constexpr uint32_t kXChunkBytes = kTileM * kRowBytes;     // one chunk of a tile
+constexpr uint32_t kRowBytes = 128;                           // 64 bf16 per smem row
+constexpr uint32_t kXChunkBytes = kTileM * kRowBytes;         // one chunk of a tile
 constexpr uint32_t kXBytes = kChunksPerStage * kXChunkBytes;  // x stage
-constexpr uint32_t kBRows = 120;                          // exact-mode B rows the MMAs read
-constexpr uint32_t kLimbRows = 4 * kMix;                  // w0..w3, 24 rows each
-constexpr uint32_t kLimbRowOffset = kMix;                 // limbs occupy B rows 24..119
-constexpr uint32_t kXTxBytes = kXBytes;
+constexpr uint32_t kLimbRows = 4 * kMix;                      // w0..w3, 24 rows each
+constexpr uint32_t kLimbRowOffset = kMix;                     // limbs occupy B rows 24..119
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACols = 64;  // exact: x0 and x1, 32 columns each; tf32x3: 64 fp32 x
-constexpr uint32_t kTf32Rows = 32;  // tf32x3 B rows per part: 24 outputs + 8 zero rows
-constexpr uint64_t kWaitLimitNs = 2000000000ull;          // 2 s per wait
+constexpr uint32_t kDCol0 = kNumA * kACols;  // first D column
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 500000000ull;
-constexpr uint32_t kWarpArrivals = 4;                      // one arrive per warp of a warpgroup
 
-struct Bookkeeping {
-  uint64_t full_x[kXStages];
-  uint64_t empty_x[kXStages];
-  uint64_t full_b[kBStages];
-  uint64_t empty_b[kBStages];
-  uint64_t a_ready[kWG];
-  uint64_t d_ready[kWG];
-  uint64_t drain[kWG];
-  uint32_t tmem_base;
-  int abort;
-  int never;  // stays 0: the abort flag of waits that must not be cut short
-};
-
-// Per-mode B buffer (one per chunk of a warpgroup's slice), MMA shape and
-// TMEM use.
+// Per-mode W buffer (one per chunk of a slot), MMA shape and D width.
 template <bool kTf32>
 struct Mode;
 template <>
 struct Mode<false> {  // exact limbs: 24 zero rows, then w0..w3 (96 rows), bf16
-  static constexpr uint32_t kBBytes = kBRows * kRowBytes;
+  static constexpr uint32_t kBBytes = (kLimbRowOffset + kLimbRows) * kRowBytes;
   static constexpr uint32_t kBTxBytes = kLimbRows * kRowBytes;
   static constexpr uint32_t kN = 96;
   static constexpr uint32_t kIdesc = sm100::idesc_bf16_f32(128, kN);
 };
 template <>
-struct Mode<true> {  // tf32x3: [big, small][two 32-column halves][32 rows][128 B], fp32
-  static constexpr uint32_t kBBytes = 2 * 2 * kTf32Rows * kRowBytes;
-  static constexpr uint32_t kBTxBytes = kBBytes;  // one TMA box, zero rows included
-  static constexpr uint32_t kN = kTf32Rows;
+struct Mode<true> {  // tf32x3: [big, small][two 32-column halves][24 rows x 128 B], fp32
+  static constexpr uint32_t kBlockBytes = kMix * kRowBytes;  // 3 KB, 1 KB aligned
+  static constexpr uint32_t kBBytes = 4 * kBlockBytes;
+  static constexpr uint32_t kBTxBytes = 0;  // no TMA path
+  // N = 32: rows 24..31 of a block are the first rows of the next one (or the
+  // shared memory after the last buffer); D columns 24..31 are never read
+  static constexpr uint32_t kN = 32;
   static constexpr uint32_t kIdesc = sm100::idesc_tf32_f32(128, kN);
 };
 template <bool kTf32>
-constexpr uint32_t kWGCols = 2 * kACols + Mode<kTf32>::kN;  // two A buffers and one D per warpgroup
-template <bool kTf32>
-constexpr size_t kRingBytes = (size_t)kXStages * kXBytes + (size_t)kBStages * Mode<kTf32>::kBBytes;
-template <bool kTf32>
-constexpr size_t kSmemBytes = kRingBytes<kTf32> + 1024 + 1024;
+constexpr uint32_t kDCols = Mode<kTf32>::kN;
 
-static_assert(kWG * kWGCols<false> <= kTmemCols && kWG * kWGCols<true> <= kTmemCols, "TMEM budget");
+template <bool kTf32>
+constexpr size_t kXOff = 0;
+template <bool kTf32>
+constexpr size_t kWOff = (size_t)kXStages * kXBytes;
+template <bool kTf32>
+constexpr size_t kSqOff = kWOff<kTf32> + (size_t)kWBufs * Mode<kTf32>::kBBytes;
+template <bool kTf32>
+constexpr size_t kBkOff = kSqOff<kTf32> + (size_t)kNumSq * kTileM * 4;
+template <bool kTf32>
+constexpr size_t kSmemBytes = kBkOff<kTf32> + 1024 + 1024;  // bookkeeping + base alignment
+
+struct Bookkeeping {
+  uint64_t full_x[kXStages];
+  uint64_t empty_x[kXStages];
+  uint64_t a_empty[kNumA];
+  uint64_t mma_ready[kNumD];  // A(k) written (4 transform warps) and D(k % 4) read (4 accumulate warps)
+  uint64_t sq_full[kNumSq];
+  uint64_t d_full[kNumD];
+  uint64_t chunk_done[kNumSq];
+  uint64_t w_full[kWBufs];
+  uint64_t drain[kNumMma];
+  uint64_t tail_bar[6];
+  uint32_t tmem_base;
+  int abort;
+  int never;  // stays 0: the abort flag of waits that must not be cut short
+};
+
+static_assert(kDCol0 + kNumD * kDCols<false> <= kTmemCols &&
+                  kDCol0 + kNumD * kDCols<true> <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Bookkeeping) <= 1024, "bookkeeping area");
-static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of one slice");
+static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of one unit");
 static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynamic shared memory");
-static_assert(Mode<false>::kBBytes % 1024 == 0 && Mode<true>::kBBytes % 1024 == 0 &&
-                  kLimbRowOffset + kLimbRows <= kBRows, "B buffer layout");
+static_assert(Mode<false>::kBBytes % 1024 == 0 && Mode<true>::kBlockBytes % 1024 == 0,
+              "W buffers keep the 1 KB swizzle atoms aligned");
+static_assert(kNumTWarps == 2 * 4 && kFirstDWarp == kFirstTWarp + kNumTWarps &&
+                  kFirstDWarp + 4 == kWarps, "warp roles");
+static_assert(kNumMma == kNumD && kNumMma == kChunksPerSlice && kFirstTWarp == 1 + kNumMma &&
+                  kNumA == 2, "issuer g owns D buffer g and W buffers (slot, g); A buffer h "
+                              "belongs to transform half h");
+
+// Parameters of one launch (passed by value as a __grid_constant__).
+struct TcParams {
+  int n_tiles;     // 128-row tiles
+  int n_slices;    // K / 256
+  int M, Mpad;
+  int64_t n_units;
+  float* part;     // workspace partials [n_slices][25][Mpad]
+  uint32_t* err;   // device error word
+  uint32_t* gbar_count, *gbar_gen;  // grid-barrier words (workspace header)
+  const float* w_src;  // fp32 W, converted in-kernel; null: limbs come by TMA
+  int64_t w_stride;
+  int tail;        // 0: partials only; 1: + mix / sq; 2: + epilogue (mix / sq optional)
+  float inv_k;
+  const float* hc_scale;
+  const float* hc_base;
+  int iters;
+  float rms_eps, hc_eps;
+  float *pre, *post, *comb, *mix_out, *sq_out;
+};
 
 // ---------------------------------------------------------------- W limbs
 
@@ -155,31 +201,34 @@ __device__ __forceinline__ uint32_t max_abs_bits16(float4 v) {
 
 // The four bf16 limbs of four consecutive W values of one (output, chunk)
 // whose largest |W| has the bit pattern m: out[p] holds limb p of the four
-// values as two packed bf16 pairs.
+// values as two packed bf16 pairs.  Pairs of values go through the packed
+// fp32 -> bf16x2 conversion together.
 __device__ __forceinline__ void split_limbs4(float4 v, uint32_t m, uint32_t (&out)[4][2]) {
   const float magic = grid_magic_from_exp_field(m >> 23);
   const float in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float w0 = grid_round(in[e], magic);
-    const float r1 = __fsub_rn(in[e], w0);
-    const float w1 = __bfloat162float(__float2bfloat16_rn(r1));
-    const float r2 = __fsub_rn(r1, w1);
-    const float w2 = __bfloat162float(__float2bfloat16_rn(r2));
-    const float w3 = __fsub_rn(r2, w2);
-    const uint32_t b[4] = {bf16_bits(w0), bf16_bits(w1), bf16_bits(w2), bf16_bits(w3)};
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      if (e % 2 == 0) out[p][e / 2] = b[p];
-      else out[p][e / 2] |= b[p] << 16;
-    }
+  for (int e = 0; e < 4; e += 2) {
+    const float2 w0 = make_float2(grid_round(in[e], magic), grid_round(in[e + 1], magic));
+    const float2 r1 = make_float2(__fsub_rn(in[e], w0.x), __fsub_rn(in[e + 1], w0.y));
+    const __nv_bfloat162 b1 = __floats2bfloat162_rn(r1.x, r1.y);
+    const float2 w1 = __bfloat1622float2(b1);
+    const float2 r2 = make_float2(__fsub_rn(r1.x, w1.x), __fsub_rn(r1.y, w1.y));
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(r2.x, r2.y);
+    const float2 w2 = __bfloat1622float2(b2);
+    const __nv_bfloat162 b3 = __floats2bfloat162_rn(__fsub_rn(r2.x, w2.x), __fsub_rn(r2.y, w2.y));
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(w0.x, w0.y);  // w0 has <= 8 bits: exact
+    out[0][e / 2] = *reinterpret_cast<const uint32_t*>(&b0);
+    out[1][e / 2] = *reinterpret_cast<const uint32_t*>(&b1);
+    out[2][e / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+    out[3][e / 2] = *reinterpret_cast<const uint32_t*>(&b3);
   }
 }
 
+// Limbs written once for hc_mix_pack_w (the pack-once API); the kernel below
+// TMA-loads them instead of converting fp32 W itself.
 __global__ void __launch_bounds__(kPackThreads)
 hcmix_pack_limbs_kernel(const float* __restrict__ W, int64_t w_stride, int K,
                         uint16_t* __restrict__ limbs) {
-  sm100::grid_launch_dependents();  // the contraction may start streaming x now
   const int sub = threadIdx.x & 15;
   const int task = blockIdx.x * kPackTasksPerBlock + (threadIdx.x >> 4);
   const int nch = K / kChunk;
@@ -198,29 +247,45 @@ hcmix_pack_limbs_kernel(const float* __restrict__ W, int64_t w_stride, int K,
         make_uint2(out[p][0], out[p][1]);
 }
 
-// W[24, K] fp32 -> parts[2][24][K] fp32 for the tf32x3 mode: part 0 is
-// big = W rounded to tf32 (nearest, ties away from zero), part 1 is
-// small = W - big, exact in fp32 and passed to the MMAs as it is (the page
-// hands the unrounded difference to its tf32 dot).  One float4 per thread.
-__global__ void __launch_bounds__(kPackThreads)
-hcmix_pack_tf32_kernel(const float* __restrict__ W, int64_t w_stride, int K,
-                       float* __restrict__ parts) {
-  sm100::grid_launch_dependents();  // the contraction may start streaming x now
-  const int64_t per_row = K / 4;
-  const int64_t i = (int64_t)blockIdx.x * kPackThreads + threadIdx.x;
-  if (i >= kMix * per_row) return;
-  const int j = (int)(i / per_row);
-  const int64_t k = (i % per_row) * 4;
-  const float4 v = *reinterpret_cast<const float4*>(W + (int64_t)j * w_stride + k);
-  const float4 big = make_float4(sm100::cvt_rna_tf32(v.x), sm100::cvt_rna_tf32(v.y),
-                                 sm100::cvt_rna_tf32(v.z), sm100::cvt_rna_tf32(v.w));
-  const float4 small = make_float4(__fsub_rn(v.x, big.x), __fsub_rn(v.y, big.y),
-                                   __fsub_rn(v.z, big.z), __fsub_rn(v.w, big.w));
-  *reinterpret_cast<float4*>(parts + (int64_t)j * K + k) = big;
-  *reinterpret_cast<float4*>(parts + (int64_t)(kMix + j) * K + k) = small;
+// One (output j, chunk) task of the in-kernel W conversion: the 16 lanes of a
+// half-warp hold four consecutive columns each (lane `sub`: columns 4 sub ..)
+// and write them into W buffer `buf` in the layout the MMAs read (128-byte
+// rows, 16-byte piece i of row r stored at piece i ^ (r & 7)).  Exact mode:
+// limb p of output j in row 24 + 24 p + j.  tf32x3 mode: big and small of
+// output j in row j of blocks [part][half].  Every lane of the warp calls it
+// (the maximum is a half-warp shuffle); `active` lanes store.
+template <bool kTf32>
+__device__ __forceinline__ void convert_w4(float4 v, int j, int sub, uint32_t buf, bool active) {
+  if constexpr (kTf32) {
+    if (!active) return;
+    const float4 big = make_float4(sm100::cvt_rna_tf32(v.x), sm100::cvt_rna_tf32(v.y),
+                                   sm100::cvt_rna_tf32(v.z), sm100::cvt_rna_tf32(v.w));
+    const float4 small = make_float4(__fsub_rn(v.x, big.x), __fsub_rn(v.y, big.y),
+                                     __fsub_rn(v.z, big.z), __fsub_rn(v.w, big.w));
+    const uint32_t half = (uint32_t)sub >> 3, piece = (uint32_t)sub & 7u, r = (uint32_t)j;
+    const uint32_t off = half * Mode<true>::kBlockBytes + r * kRowBytes + ((piece ^ (r & 7u)) << 4);
+    sm100::sts128(buf + off, make_uint4(__float_as_uint(big.x), __float_as_uint(big.y),
+                                        __float_as_uint(big.z), __float_as_uint(big.w)));
+    sm100::sts128(buf + 2 * Mode<true>::kBlockBytes + off,
+                  make_uint4(__float_as_uint(small.x), __float_as_uint(small.y),
+                             __float_as_uint(small.z), __float_as_uint(small.w)));
+  } else {
+    const uint32_t m = max_abs_bits16(v);
+    if (!active) return;
+    uint32_t out[4][2];
+    split_limbs4(v, m, out);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t r = kLimbRowOffset + (uint32_t)(p * kMix + j);
+      const uint32_t addr =
+          buf + r * kRowBytes + ((((uint32_t)sub >> 1) ^ (r & 7u)) << 4) + ((uint32_t)sub & 1u) * 8;
+      asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(out[p][0]), "r"(out[p][1])
+                   : "memory");
+    }
+  }
 }
 
-// ---------------------------------------------------------------- main kernel
+// ---------------------------------------------------------------- x transform
 
 constexpr uint32_t kBf16x2One = 0x3f803f80u;
 
@@ -270,10 +335,12 @@ __device__ __forceinline__ float sq_tree64_f32x2(const uint32_t (&w)[32]) {
   return __fadd_rn(h[0], h[1]);                                      // the two halves
 }
 
+// ---------------------------------------------------------------- MMA issue
+
 // One chunk's MMAs and the commit to `bar` from one asm block: the whole
 // (converged) warp runs it and the lane that elect.sync picks issues every
 // instruction, so the issuer spends a few instructions per MMA.  `a` is the
-// chunk's TMEM A buffer, `bdesc` the descriptor of its B buffer; a K-step
+// chunk's TMEM A buffer, `bdesc` the descriptor of its W buffer; a K-step
 // advances the B start address by 32 bytes (2 descriptor units).
 //
 // Exact limbs: x1 (A columns 32..63) against B rows 0..95 = [0 | w0 | w1 | w2]
@@ -319,8 +386,8 @@ __device__ __forceinline__ void mma_chunk_exact(uint32_t d, uint32_t a, uint64_t
 }
 
 // tf32x3: dot(x, small) from zero, then + dot(x, big); eight K-steps of 8
-// columns each (A columns 8q..), K-step q in half q / 4 (+4096 bytes = 256
-// units) at 32 bytes per step, the small part 8192 bytes (512 units) after
+// columns each (A columns 8q..), K-step q in half q / 4 (+3072 bytes = 192
+// units) at 32 bytes per step, the small part 6144 bytes (384 units) after
 // the big one.
 __device__ __forceinline__ void mma_chunk_tf32x3(uint32_t d, uint32_t a, uint64_t bdesc,
                                                  uint32_t idesc, uint32_t bar) {
@@ -333,28 +400,28 @@ __device__ __forceinline__ void mma_chunk_tf32x3(uint32_t d, uint32_t a, uint64_
       "setp.eq.b32 pa, %1, %1;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "add.u32 ta, %1, 0;\n\t"
-      "add.u64 tb, %2, 512;\n\t"
+      "add.u64 tb, %2, 384;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pz;\n\t"
       "add.u32 ta, %1, 8;\n\t"
-      "add.u64 tb, %2, 514;\n\t"
+      "add.u64 tb, %2, 386;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 16;\n\t"
-      "add.u64 tb, %2, 516;\n\t"
+      "add.u64 tb, %2, 388;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 24;\n\t"
-      "add.u64 tb, %2, 518;\n\t"
+      "add.u64 tb, %2, 390;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 32;\n\t"
-      "add.u64 tb, %2, 768;\n\t"
+      "add.u64 tb, %2, 576;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 40;\n\t"
-      "add.u64 tb, %2, 770;\n\t"
+      "add.u64 tb, %2, 578;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 48;\n\t"
-      "add.u64 tb, %2, 772;\n\t"
+      "add.u64 tb, %2, 580;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 56;\n\t"
-      "add.u64 tb, %2, 774;\n\t"
+      "add.u64 tb, %2, 582;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 0;\n\t"
       "add.u64 tb, %2, 0;\n\t"
@@ -369,20 +436,28 @@ __device__ __forceinline__ void mma_chunk_tf32x3(uint32_t d, uint32_t a, uint64_
       "add.u64 tb, %2, 6;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 32;\n\t"
-      "add.u64 tb, %2, 256;\n\t"
+      "add.u64 tb, %2, 192;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 40;\n\t"
-      "add.u64 tb, %2, 258;\n\t"
+      "add.u64 tb, %2, 194;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 48;\n\t"
-      "add.u64 tb, %2, 260;\n\t"
+      "add.u64 tb, %2, 196;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "add.u32 ta, %1, 56;\n\t"
-      "add.u64 tb, %2, 262;\n\t"
+      "add.u64 tb, %2, 198;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [ta], tb, %3, pa;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}"
       ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(bar)
       : "memory");
+}
+
+// CTA-wide barrier for code in which the lanes of a warp have taken
+// different paths (one lane producing, the others idle): the warp first
+// reconverges, so that the barrier sees whole warps, as it requires.
+__device__ __forceinline__ void cta_barrier() {
+  __syncwarp();
+  __syncthreads();
 }
 
 __device__ __forceinline__ void fail(Bookkeeping& bk, uint32_t* err) {
@@ -390,329 +465,381 @@ __device__ __forceinline__ void fail(Bookkeeping& bk, uint32_t* err) {
   *reinterpret_cast<volatile int*>(&bk.abort) = 1;
 }
 
+// Grid-wide barrier on two words of the workspace header, called by one
+// thread per CTA after a CTA barrier that follows the CTA's stores.  The
+// arrival is a release at GPU scope (it publishes the CTA's stores); the last
+// CTA to arrive puts the count back to zero and moves the generation on with a
+// release, and the others wait, bounded, for the generation to move with
+// acquire loads.  Every CTA must be resident (cooperative launch).  Returns
+// false when the wait ran out.
+__device__ __forceinline__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t nblocks,
+                                             uint64_t limit_ns) {
+  const uint32_t g0 = sm100::ld_acquire_gpu(gen);  // before arriving: the last arrival moves it
+  if (sm100::atom_add_release_gpu(count, 1u) == nblocks - 1) {
+    *reinterpret_cast<volatile uint32_t*>(count) = 0u;
+    sm100::red_add_release_gpu(gen, 1u);  // also orders the reset before the next launch's arrivals
+    return true;
+  }
+  const uint64_t t0 = sm100::global_timer_ns();
+  for (uint32_t i = 0; sm100::ld_acquire_gpu(gen) == g0; ++i) {
+    if ((i & 63u) == 63u && sm100::global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- partials
+
+// The tensor-core path stores the slice totals of 8-row groups ("octs")
+// contiguously, so that the rows a CTA reduces arrive in a few bulk copies:
+// value j (24 mix values, then the sum of squares) of slice s for row r sits at
+//   part[((r / 8 * n_slices + s) * 25 + j) * 8 + r % 8].
+// A warp's 32 rows of one (s, j) are four full 32-byte sectors.
+__device__ __forceinline__ int64_t part_index(int row, int s, int j, int n_slices) {
+  return ((int64_t)(row >> 3) * n_slices + s) * (kPartStride * 8) + j * 8 + (row & 7);
+}
+
+constexpr int kTailSlices = 40;                                      // slices per bulk copy
+constexpr uint32_t kTailSlotBytes = kTailSlices * kPartStride * 8 * 4;  // 32000
+constexpr int kTailSlotsPerHalf = 3;
+constexpr int kTailSlots = 2 * kTailSlotsPerHalf;                    // three per half of the CTA
+constexpr size_t kTailTotOff = (size_t)kTailSlots * kTailSlotBytes;
+constexpr size_t kTailParOff = kTailTotOff + (size_t)kPartStride * (kReduceRows + 1) * 4;
+constexpr size_t kTailBytes = (kTailParOff + 32 * 4 + 15) / 16 * 16;  // shared memory the tail uses
+constexpr int kTailThreads = 512;
+
+// The tail of a call for CTA b of G: the octs [b n / G, (b + 1) n / G) of the
+// n = ceil(M / 8) octs.  Each half of the CTA (256 threads) takes every other
+// oct; its thread t < 200 owns value j = t / 8 of row t % 8 and adds that
+// value's slice totals in slice order from zero, reading them from bulk
+// copies of up to 40 slices (three slots per half, all in flight from the
+// start, each refilled once added up).  Every 4 octs (32 rows) the CTA writes
+// mix / sq (when asked for) and, with P.tail == 2, runs the epilogue on those
+// rows, one thread per row.  `tb`: kTailBytes of shared memory (16-byte
+// aligned); `tbar`: kTailSlots mbarriers;
+// `never`: a flag that stays 0 (the waits here are bounded by time only).
+__device__ __forceinline__ void tc_tail(const TcParams& P, uint8_t* tb, uint64_t* tbar,
+                                        const volatile int* never, int64_t b, int64_t G) {
+  using namespace sm100;
+  const int tid = threadIdx.x;
+  const int n_octs = (P.M + 7) / 8;
+  const int o0 = (int)(b * n_octs / G), o1 = (int)((b + 1) * n_octs / G);
+  auto& s_tot = *reinterpret_cast<float (*)[kPartStride][kReduceRows + 1]>(tb + kTailTotOff);
+  float* s_par = reinterpret_cast<float*>(tb + kTailParOff);  // hc_scale[3], hc_base[24]
+  if (P.tail == 2 && tid < 3 + kMix) s_par[tid] = tid < 3 ? P.hc_scale[tid] : P.hc_base[tid - 3];
+  const int ns = P.n_slices;
+  const int n_pieces = (ns + kTailSlices - 1) / kTailSlices;
+  // threads past the two halves (the kernel has a warp more) only join the CTA barriers
+  const int h = min(tid >> 8, 2), t = tid & 255;
+  const int my_octs = h < 2 && o1 - o0 > h ? (o1 - o0 - h + 1) / 2 : 0;  // octs o0 + h, o0 + h + 2, ...
+  const int n_items = my_octs * n_pieces;                       // item = (oct, piece)
+  const uint32_t slot0 = smem_u32(tb) + (uint32_t)(kTailSlotsPerHalf * min(h, 1)) * kTailSlotBytes;
+  const uint32_t bar0 = smem_u32(&tbar[kTailSlotsPerHalf * min(h, 1)]);
+  auto issue = [&](int i) {  // item i of this half into its slot i % 3
+    const int oct = o0 + h + 2 * (i / n_pieces), s0 = (i % n_pieces) * kTailSlices;
+    const uint32_t bytes = (uint32_t)min(kTailSlices, ns - s0) * (kPartStride * 8 * 4);
+    const uint32_t bar = bar0 + (uint32_t)(i % kTailSlotsPerHalf) * 8;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(slot0 + (uint32_t)(i % kTailSlotsPerHalf) * kTailSlotBytes,
+              P.part + ((int64_t)oct * ns + s0) * (kPartStride * 8), bytes, bar,
+              l2_policy_evict_first());
+  };
+  if (tid == 0) {
+    for (int q = 0; q < kTailSlots; ++q) mbar_init(smem_u32(&tbar[q]), 1);
+    fence_mbarrier_init();
+  }
+  cta_barrier();
+  if (t == 0 && h < 2) {
+    // the partials were written by other CTAs through the generic proxy
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    for (int i = 0; i < kTailSlotsPerHalf && i < n_items; ++i) issue(i);
+  }
+  const int j = t >> 3, r8 = t & 7;
+  const int n_groups = (o1 - o0 + 3) / 4;
+  int i = 0;
+  for (int g = 0; g < n_groups; ++g) {
+    for (int q = 0; q < 2; ++q) {
+      const int m = 2 * g + q;  // this half's m-th oct
+      if (m >= my_octs) continue;
+      float tot = 0.0f;
+      for (int p = 0; p < n_pieces; ++p, ++i) {
+        if (!mbar_wait(bar0 + (uint32_t)(i % kTailSlotsPerHalf) * 8,
+                       (uint32_t)(i / kTailSlotsPerHalf) & 1u, never, kWaitLimitNs))
+          record_device_error(P.err, kDevWaitTimeout);
+        if (t < kPartStride * 8) {
+          const float* v = reinterpret_cast<const float*>(
+              tb + (size_t)(kTailSlotsPerHalf * h + i % kTailSlotsPerHalf) * kTailSlotBytes);
+          const int cnt = min(kTailSlices, ns - p * kTailSlices);
+#pragma unroll 8
+          for (int s = 0; s < cnt; ++s) tot = __fadd_rn(tot, v[(s * kPartStride + j) * 8 + r8]);
+        }
+        named_bar_sync(1 + h, 256);  // the half has read the slot
+        if (t == 0 && i + kTailSlotsPerHalf < n_items) issue(i + kTailSlotsPerHalf);
+      }
+      if (t < kPartStride * 8) s_tot[j][(h + 2 * q) * 8 + r8] = tot;
+    }
+    cta_barrier();
+    const int r0 = (o0 + 4 * g) * 8;
+    const int nr = min(min(32, (o1 - o0 - 4 * g) * 8), P.M - r0);
+    if (P.mix_out != nullptr)
+      for (int e = tid; e < nr * kMix; e += kTailThreads)
+        P.mix_out[(int64_t)(r0 + e / kMix) * kMix + e % kMix] = s_tot[e % kMix][e / kMix];
+    if (P.sq_out != nullptr && tid < nr) P.sq_out[r0 + tid] = s_tot[kMix][tid];
+    if (P.tail == 2)
+      epilogue_rows(s_tot, r0, nr, r0 + nr, P.inv_k, s_par, s_par + 3, P.iters, P.rms_eps,
+                    P.hc_eps, P.pre, P.post, P.comb);
+    cta_barrier();
+  }
+}
+
+// ---------------------------------------------------------------- the kernel
+
 template <bool kTf32>
 __global__ void __launch_bounds__(kThreads, 1)
 hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                const __grid_constant__ CUtensorMap tmap_w, int n_tiles, int Mpad,
-                int64_t n_units, float* __restrict__ part, uint32_t* __restrict__ err,
-                const float* __restrict__ w_src, int64_t w_stride) {
+                const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ TcParams P) {
   using namespace sm100;
+  using MD = Mode<kTf32>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  using MD = Mode<kTf32>;
-  constexpr uint32_t kWGC = kWGCols<kTf32>;
-  Bookkeeping& bk = *reinterpret_cast<Bookkeeping*>(smem + kRingBytes<kTf32>);
+  Bookkeeping& bk = *reinterpret_cast<Bookkeeping*>(smem + kBkOff<kTf32>);
+  float* sq_buf = reinterpret_cast<float*>(smem + kSqOff<kTf32>);  // [kNumSq][128]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int64_t G = gridDim.x, b = blockIdx.x;
-  const int64_t u_begin = b * n_units / G;
-  const int n = (int)((b + 1) * n_units / G - u_begin);
+  const int64_t u_begin = b * P.n_units / G;
+  const int n = (int)((b + 1) * P.n_units / G - u_begin);  // units of this CTA, >= 1
+  const int n_chunks = kChunksPerSlice * n;
+  const int n_loads = n_chunks / kChunksPerStage;
+  const int s_first = (int)(u_begin / P.n_tiles);
+  const int n_sl = (int)((u_begin + n - 1) / P.n_tiles) - s_first + 1;  // slices of this CTA
 
-  auto x_smem = [&](int st) { return smem + (size_t)st * kXBytes; };
-  auto b_smem = [&](int st) { return smem + (size_t)kXStages * kXBytes + (size_t)st * MD::kBBytes; };
+  const uint32_t x_base = smem_u32(smem + kXOff<kTf32>);
+  const uint32_t w_base = smem_u32(smem + kWOff<kTf32>);
+  auto wbuf = [&](int slot, int c) {
+    return w_base + (uint32_t)(slot * kChunksPerSlice + c) * MD::kBBytes;
+  };
+  // unit i of this CTA: tile (u % n_tiles) of slice (u / n_tiles), u = u_begin + i
+  auto unit_tile = [&](int i) { return (int)((u_begin + i) % P.n_tiles); };
+  auto unit_slice = [&](int i) { return (int)((u_begin + i) / P.n_tiles); };
 
-  // units are slice-major: unit u is tile u % n_tiles of slice u / n_tiles
-  auto unit_tile = [&](int64_t u) { return (int)(u % n_tiles); };
-  auto unit_slice = [&](int64_t u) { return (int)(u / n_tiles); };
-
-  // x loads in the producer's order (round, chunk pair, warpgroup); load i
-  // fills stage i % kXStages, each stage two chunks of one unit, released by
-  // its warpgroup.  Issues the loads numbered [from, to) and returns how many
-  // loads were issued in total; ok turns false when a wait for a free stage
-  // gives up.  Loads below kXStages need no free stage.
-  auto x_loads = [&](int from, int to, uint64_t pol, const volatile int* abort_flag,
-                     bool& ok) -> int {
-    int i = 0;
-    for (int r = 0; kWG * r < n; ++r) {
-      const int act = min(kWG, n - kWG * r);
-      for (int c = 0; c < kChunksPerSlice; c += kChunksPerStage) {
-        for (int g = 0; g < act; ++g, ++i) {
-          if (i < from) continue;
-          if (i >= to) return i;
-          const int64_t unit = u_begin + kWG * r + g;
-          const int st = i % kXStages;
-          const uint32_t ph = (uint32_t)(i / kXStages) & 1u;
-          if (i >= kXStages &&
-              !mbar_wait(smem_u32(&bk.empty_x[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
-            ok = false;
-            return i;
-          }
-          const uint32_t full = smem_u32(&bk.full_x[st]);
-          mbar_arrive_expect_tx(full, kXTxBytes);
-          tma_load_3d(smem_u32(x_smem(st)), &tmap_x, 0, unit_tile(unit) * kTileM,
-                      unit_slice(unit) * kChunksPerSlice + c, full, pol);
+  // x load L fills stage L % kXStages with chunks 2L and 2L + 1 (unit L / 2)
+  auto issue_x_load = [&](int L, uint64_t pol) {
+    const int st = L % kXStages, i = L / 2;
+    const uint32_t full = smem_u32(&bk.full_x[st]);
+    mbar_arrive_expect_tx(full, kXBytes);
+    tma_load_3d(x_base + (uint32_t)st * kXBytes, &tmap_x, 0, unit_tile(i) * kTileM,
+                unit_slice(i) * kChunksPerSlice + (L % 2) * kChunksPerStage, full, pol);
+  };
+  // limbs of chunk c of slice s into W buffer (slot, c) by TMA (exact mode)
+  auto issue_w_load = [&](int slot, int c, int s, uint64_t pol) {
+    const uint32_t full = smem_u32(&bk.w_full[slot * kChunksPerSlice + c]);
+    mbar_arrive_expect_tx(full, MD::kBTxBytes);
+    tma_load_2d(wbuf(slot, c) + kLimbRowOffset * kRowBytes, &tmap_w, (s * kChunksPerSlice + c) * kChunk,
+                0, full, pol);
+  };
+  // the fp32 W of slice index j (slot j % 2), converted by the `nthreads`
+  // threads numbered `tid` from 0, all of a thread's W loads in flight at once
+  // (with `zero`, the zero rows of the exact-mode W buffers are written while
+  // they are on their way)
+  auto convert_slice = [&](int j, int tid, int nthreads, bool zero) {
+    constexpr int kTasks = kMix * kChunksPerSlice;  // (output, chunk) pairs, 16 lanes each
+    const int groups = nthreads / 16, sub = tid & 15;
+    constexpr int kMaxRounds = 12;  // 96 tasks over at least 8 groups
+    float4 wv[kMaxRounds];
+#pragma unroll
+    for (int q = 0; q < kMaxRounds; ++q) {
+      const int task = q * groups + (tid >> 4);
+      wv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (task < kTasks)
+        wv[q] = *reinterpret_cast<const float4*>(
+            P.w_src + (int64_t)(task / kChunksPerSlice) * P.w_stride +
+            (int64_t)(s_first + j) * kSlice + (task % kChunksPerSlice) * kChunk + 4 * sub);
+    }
+    if constexpr (!kTf32) {
+      if (zero) {
+        constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
+        for (int idx = tid; idx < kWBufs * kUnits; idx += nthreads) {
+          const int w = idx / kUnits, u = idx % kUnits;
+          sts128(w_base + (uint32_t)w * MD::kBBytes + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
         }
       }
     }
-    return i;
+#pragma unroll
+    for (int q = 0; q < kMaxRounds; ++q) {  // uniform trip count: the shuffles need whole warps
+      const int task = q * groups + (tid >> 4);
+      if (q * groups >= kTasks) break;
+      const bool active = task < kTasks;
+      const int t = active ? task : 0;
+      convert_w4<kTf32>(wv[q], t / kChunksPerSlice, sub, wbuf(j % kSlots, t % kChunksPerSlice),
+                        active);
+    }
   };
 
-  // ---- set-up: barriers, the zero rows of every B buffer, TMEM.  Thread 0,
-  // which is also the x producer, starts the first x loads as soon as the
-  // barriers exist, so their DRAM latency overlaps the rest of the set-up.
+  // ---- set-up.  Thread 0 initialises the barriers and starts the first x
+  // loads (and, with prepacked limbs, the W loads of the first two slices);
+  // warp 1 allocates TMEM; warps 2..15 zero the W buffers' zero rows and
+  // convert the first slice's fp32 W, while the first x loads are in flight.
   if (threadIdx.x == 0) {
+    // the x barriers first, so that the first x loads leave at once
     for (int s = 0; s < kXStages; ++s) {
       mbar_init(smem_u32(&bk.full_x[s]), 1);
-      mbar_init(smem_u32(&bk.empty_x[s]), kWarpArrivals);
+      mbar_init(smem_u32(&bk.empty_x[s]), kNumTWarps);
     }
-    for (int s = 0; s < kBStages; ++s) {
-      mbar_init(smem_u32(&bk.full_b[s]), 1);
-      mbar_init(smem_u32(&bk.empty_b[s]), 1);
+    fence_mbarrier_init();
+    {
+      const uint64_t pol = l2_policy_evict_first();
+      for (int L = 0; L < kXStages && L < n_loads; ++L) issue_x_load(L, pol);
     }
-    for (int g = 0; g < kWG; ++g) {
-      mbar_init(smem_u32(&bk.a_ready[g]), kWarpArrivals);
-      mbar_init(smem_u32(&bk.d_ready[g]), 1);
+    // mma_ready[k % 4]: the four transform warps of chunk k and the four
+    // accumulate warps once they have read chunk k - 4 (for the first four
+    // chunks, those four arrivals are made here)
+    for (int d = 0; d < kNumD; ++d) {
+      mbar_init(smem_u32(&bk.mma_ready[d]), 8);
+      for (int q = 0; q < 4; ++q) mbar_arrive(smem_u32(&bk.mma_ready[d]));
     }
-    for (int g = 0; g < kWG; ++g) mbar_init(smem_u32(&bk.drain[g]), 1);
+    for (int a = 0; a < kNumA; ++a) mbar_init(smem_u32(&bk.a_empty[a]), 1);  // MMA commit
+    for (int d = 0; d < kNumD; ++d) mbar_init(smem_u32(&bk.d_full[d]), 1);  // MMA commit
+    for (int q = 0; q < kNumSq; ++q) {
+      mbar_init(smem_u32(&bk.sq_full[q]), 4);     // the four transform warps of the chunk
+      mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the four accumulate warps
+    }
+    for (int w = 0; w < kWBufs; ++w) mbar_init(smem_u32(&bk.w_full[w]), 1);
+    for (int g = 0; g < kNumMma; ++g) mbar_init(smem_u32(&bk.drain[g]), 1);
     bk.abort = 0;
     bk.never = 0;
     fence_mbarrier_init();
-    prefetch_tensormap(&tmap_x);
-    bool ok = true;
-    x_loads(0, kXStages, l2_policy_evict_first(), &bk.never, ok);
-  }
-  if constexpr (!kTf32) {
-    // rows 0..23 of each B buffer stay zero (the limbs are loaded to rows 24..119;
-    // the tf32x3 boxes bring their own zero rows)
-    constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
-    for (int idx = threadIdx.x; idx < kBStages * kUnits; idx += kThreads) {
-      const int s = idx / kUnits, u = idx % kUnits;
-      sts128(smem_u32(b_smem(s)) + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
-    }
-    if (w_src != nullptr) {
-      // every CTA owns one unit (small batches): the whole CTA splits that
-      // unit's slice of W straight into warpgroup 0's four B buffers, in the
-      // layout the TMA would give (row r of a buffer: 128 bytes, 16-byte
-      // piece i stored at piece i ^ (r & 7)), instead of a separate pack
-      // kernel writing limbs for every slice
-      const int64_t k_slice = (int64_t)(u_begin / n_tiles) * kSlice;
-      const int sub = threadIdx.x & 15;
-      constexpr int kTasks = kMix * kChunksPerSlice;  // (output, chunk) pairs, 16 lanes each
-      constexpr int kGroups = kThreads / 16;
-      constexpr int kRounds = (kTasks + kGroups - 1) / kGroups;
-      float4 wv[kRounds];  // every W load of this lane in flight at once
-#pragma unroll
-      for (int q = 0; q < kRounds; ++q) {
-        const int task = q * kGroups + (threadIdx.x >> 4);
-        wv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (task < kTasks)
-          wv[q] = *reinterpret_cast<const float4*>(
-              w_src + (int64_t)(task / kChunksPerSlice) * w_stride + k_slice +
-              (task % kChunksPerSlice) * kChunk + 4 * sub);
-      }
-#pragma unroll
-      for (int q = 0; q < kRounds; ++q) {  // uniform trip count
-        const int task = q * kGroups + (threadIdx.x >> 4);
-        const bool active = task < kTasks;
-        const int j = active ? task / kChunksPerSlice : 0, c = active ? task % kChunksPerSlice : 0;
-        const float4 v = wv[q];
-        const uint32_t m = max_abs_bits16(v);
-        if (!active) continue;
-        uint32_t out[4][2];
-        split_limbs4(v, m, out);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const uint32_t r = kLimbRowOffset + (uint32_t)(p * kMix + j);
-          const uint32_t addr = smem_u32(b_smem(c)) + r * kRowBytes +
-                                ((((uint32_t)sub >> 1) ^ (r & 7u)) << 4) + ((uint32_t)sub & 1u) * 8;
-          asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(out[p][0]),
-                       "r"(out[p][1])
-                       : "memory");
-        }
+    if constexpr (!kTf32) {
+      if (P.w_src == nullptr) {
+        prefetch_tensormap(&tmap_w);
+        const uint64_t wpol = l2_policy_evict_last();
+        for (int j = 0; j < kSlots && j < n_sl; ++j)
+          for (int c = 0; c < kChunksPerSlice; ++c) issue_w_load(j, c, s_first + j, wpol);
       }
     }
-    fence_proxy_async_smem();
-  }
-  if (warp == 1) {
+  } else if (warp == kMmaWarp0) {
     tmem_alloc(smem_u32(&bk.tmem_base), kTmemCols);
     tmem_relinquish();
+  } else if (warp >= 2) {
+    const int tid = threadIdx.x - 64, nthr = kThreads - 64;
+    if (P.w_src != nullptr) {
+      convert_slice(0, tid, nthr, true);
+    } else if constexpr (!kTf32) {  // prepacked limbs: only the zero rows
+      constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
+      for (int idx = tid; idx < kWBufs * kUnits; idx += nthr) {
+        const int w = idx / kUnits, u = idx % kUnits;
+        sts128(w_base + (uint32_t)w * MD::kBBytes + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
+      }
+    }
+    fence_proxy_async_smem();  // generic-proxy stores -> the MMAs' (async proxy) reads
   }
   tc_fence_before();
-  __syncthreads();
+  cta_barrier();
   tc_fence_after();
+  if (threadIdx.x == 0 && P.w_src != nullptr)  // the first slice is in place
+    for (int c = 0; c < kChunksPerSlice; ++c) mbar_arrive(smem_u32(&bk.w_full[c]));
   const uint32_t tmem = bk.tmem_base;
   const volatile int* abort_flag = &bk.abort;
   const volatile int* never = &bk.never;
 
-  if (warp == 0) {
-    // ---------------- x producer (thread 0): the loads after the first
-    // kXStages, each once its stage has been released
+  if (warp == kXWarp) {
+    // ---------------- x producer: the loads after the first kXStages, each
+    // once the transform warps of its stage have read it
     if (lane == 0) {
-      bool ok = true;
-      const int i = x_loads(kXStages, 1 << 30, l2_policy_evict_first(), abort_flag, ok);
-      if (!ok) fail(bk, err);
+      const uint64_t pol = l2_policy_evict_first();
+      int L = kXStages;
+      for (; L < n_loads; ++L) {
+        const int st = L % kXStages;
+        if (!mbar_wait(smem_u32(&bk.empty_x[st]), ((uint32_t)(L / kXStages) & 1u) ^ 1u, abort_flag,
+                       kWaitLimitNs)) {
+          fail(bk, P.err);
+          break;
+        }
+        issue_x_load(L, pol);
+      }
       // drain: the loads still in flight complete before the CTA can exit
-      for (int j = max(0, i - kXStages); j < i; ++j)
+      for (int j = max(0, min(L, n_loads) - kXStages); j < min(L, n_loads); ++j)
         mbar_wait(smem_u32(&bk.full_x[j % kXStages]), (uint32_t)(j / kXStages) & 1u, never,
                   kDrainLimitNs);
     }
-  } else if (warp == 2) {
-    // ---------------- W producer: when warpgroup g reaches a new slice, its
-    // four B buffers are reloaded with that slice's limbs, once the MMAs of
-    // its previous slice have released them (empty_b, committed after their
-    // last use)
-    if (lane == 0 && w_src != nullptr) {
-      // the set-up filled warpgroup 0's buffers with the CTA's only slice
-      for (int c = 0; c < kChunksPerSlice; ++c) mbar_arrive(smem_u32(&bk.full_b[c]));
-    } else if (lane == 0) {
-      prefetch_tensormap(&tmap_w);
-      grid_dependency_wait();  // the limbs come from the pack kernel launched before
-      const uint64_t pol = l2_policy_evict_last();
-      int loads[kWG] = {0, 0}, cur[kWG] = {-1, -1};
-      bool ok = true;
-      for (int r = 0; ok && kWG * r < n; ++r) {
-        const int act = min(kWG, n - kWG * r);
-#pragma unroll
-        for (int g = 0; g < kWG; ++g) {
-          if (!ok || g >= act) continue;
-          const int sl = unit_slice(u_begin + kWG * r + g);
-          if (sl == cur[g]) continue;
-          cur[g] = sl;
-          for (int c = 0; c < kChunksPerSlice; ++c) {
-            const int j = g * kChunksPerSlice + c;
-            if (loads[g] > 0 && !mbar_wait(smem_u32(&bk.empty_b[j]),
-                                           (uint32_t)(loads[g] - 1) & 1u, abort_flag,
-                                           kWaitLimitNs)) {
-              fail(bk, err);
-              ok = false;
-              break;
-            }
-            const uint32_t full = smem_u32(&bk.full_b[j]);
-            mbar_arrive_expect_tx(full, MD::kBTxBytes);
-            if constexpr (kTf32)  // both parts, both 32-column halves of the chunk
-              tma_load_4d(smem_u32(b_smem(j)), &tmap_w, 0, 0,
-                          2 * (sl * kChunksPerSlice + c), 0, full, pol);
-            else
-              tma_load_2d(smem_u32(b_smem(j)) + kLimbRowOffset * kRowBytes, &tmap_w,
-                          (sl * kChunksPerSlice + c) * kChunk, 0, full, pol);
-          }
-          ++loads[g];
-        }
-      }
-      // drain
-#pragma unroll
-      for (int g = 0; g < kWG; ++g)
-        if (loads[g] > 0)
-          for (int c = 0; c < kChunksPerSlice; ++c)
-            mbar_wait(smem_u32(&bk.full_b[g * kChunksPerSlice + c]), (uint32_t)(loads[g] - 1) & 1u,
-                      never, kDrainLimitNs);
-    }
-  } else if (warp == 1 || warp == kMmaWarp1) {
-    // ---------------- MMA issuer of warpgroup gm, its chunks in sequence
-    // order (round, chunk).  One issuer per warpgroup: an issuing thread
-    // spends ~45 cycles per MMA and, once MMAs are queued, a few hundred
-    // cycles in any shared-memory access (its mbarrier waits included), so a
-    // single issuer for both warpgroups left the tensor pipe idle between
-    // chunks.  Each commit tracks the MMAs of the thread that issues it, so
-    // the two issuers' commits are independent.  Chunk i needs its
-    // warpgroup's x limbs (a_ready) and the W limb tile of its slice (full_b,
-    // phase = the warpgroup's slice count).  In order, each wait depends only
-    // on earlier chunks, so no wait can close a cycle.  The whole warp runs the loop, the waits are warp votes and one
-    // elected lane issues each MMA and commit: a loop whose control flow the
-    // compiler cannot prove warp-uniform issued MMAs at about half the rate.
-    // per warpgroup: slice of its current unit, B loads so far, and whether
-    // this round's unit is the last of its slice (tracked incrementally: the
-    // units of a round are consecutive)
-    const int gm = warp == 1 ? 0 : 1;
-    int64_t u_tile = u_begin % n_tiles, u_slice = u_begin / n_tiles;  // of unit u_begin + kWG * r
-    int loads[kWG] = {0, 0}, cur[kWG] = {-1, -1};
+  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kNumMma) {
+    // ---------------- MMA issuers: warp 1 + c issues chunk c of every unit,
+    // into D buffer c with W buffer (slot, c).  An issuing thread's
+    // shared-memory accesses, its mbarrier waits included, wait behind the
+    // MMAs it has queued, so one issuer cannot queue its next chunk before its
+    // previous one completes; four take turns and keep the tensor pipe busy.
+    // Chunk k needs its A buffer written and its D buffer read (both on
+    // mma_ready, one poll) and, in the first unit of a slice, its W buffer
+    // filled (w_full).  Each barrier it waits on is its own, so it has seen
+    // every earlier phase, as a parity wait needs.  Each chunk commits twice:
+    // D complete (d_full) and A free again (a_empty).  The whole warp runs
+    // the loop, the waits are warp votes and one elected lane issues each MMA
+    // and commit.
+    const int c = warp - kMmaWarp0;
     bool ok = true;
-    for (int r = 0; ok && kWG * r < n; ++r) {
-      const int act = min(kWG, n - kWG * r);
-      int sl[kWG];
-      bool fresh[kWG], last_use[kWG];
-      {
-        int64_t t = u_tile, sv = u_slice;
-#pragma unroll
-        for (int g = 0; g < kWG; ++g) {
-          sl[g] = (int)sv;
-          fresh[g] = g < act && sl[g] != cur[g];
-          if (fresh[g]) {
-            cur[g] = sl[g];
-            ++loads[g];
-          }
-          if (++t == n_tiles) { t = 0; ++sv; }
-        }
-        u_tile = t;
-        u_slice = sv;
-        // unit + kWG of warpgroup g is unit kWG * (r + 1) + g: its slice
-#pragma unroll
-        for (int g = 0; g < kWG; ++g) {
-          int64_t t2 = t, s2 = sv;
-          for (int q = 0; q < g; ++q)
-            if (++t2 == n_tiles) { t2 = 0; ++s2; }
-          last_use[g] = kWG * (r + 1) + g >= n || (int)s2 != sl[g];
-        }
-      }
-      for (int c = 0; ok && c < kChunksPerSlice; ++c) {
-#pragma unroll
-        for (int g = 0; g < kWG; ++g) {
-          if (!ok || g >= act || g != gm) continue;
-          const int j = g * kChunksPerSlice + c;
-          const uint32_t aph = (uint32_t)(r * kChunksPerSlice + c) & 1u;
-          // the W buffer is waited for at its first use in a slice only
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(smem_u32(&bk.a_ready[g]), aph, abort_flag, kWaitLimitNs) &&
-                              (!fresh[g] ||
-                               mbar_wait(smem_u32(&bk.full_b[j]), (uint32_t)(loads[g] - 1) & 1u,
-                                         abort_flag, kWaitLimitNs)));
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t a = tmem + (uint32_t)g * kWGC + aph * kACols;
-          const uint32_t d = tmem + (uint32_t)g * kWGC + 2 * kACols;
-          const uint64_t bdesc = smem_desc_sw128(smem_u32(b_smem(j)));
-          if constexpr (kTf32)
-            mma_chunk_tf32x3(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_ready[g]));
-          else
-            mma_chunk_exact(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_ready[g]));
-          if (last_use[g]) umma_commit_warp(smem_u32(&bk.empty_b[j]));
-        }
-      }
+    int prev_slice = -1;
+    for (int i = 0; ok && i < n; ++i) {
+      const int k = kChunksPerSlice * i + c;
+      const int s = unit_slice(i), j = s - s_first, slot = j % kSlots;
+      const bool first_use = s != prev_slice;
+      prev_slice = s;
+      bool got = mbar_wait(smem_u32(&bk.mma_ready[c]), (uint32_t)i & 1u, abort_flag, kWaitLimitNs);
+      if (first_use)
+        got = got && mbar_wait(smem_u32(&bk.w_full[slot * kChunksPerSlice + c]),
+                               (uint32_t)(j / kSlots) & 1u, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, got);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a = tmem + (uint32_t)(k % kNumA) * kACols;
+      const uint32_t d = tmem + kDCol0 + (uint32_t)c * kDCols<kTf32>;
+      const uint64_t bdesc = smem_desc_sw128(wbuf(slot, c));
+      if constexpr (kTf32)
+        mma_chunk_tf32x3(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[c]));
+      else
+        mma_chunk_exact(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[c]));
+      umma_commit_warp(smem_u32(&bk.a_empty[k % kNumA]));
     }
-    if (!ok && lane == 0) fail(bk, err);
-    umma_commit_warp(smem_u32(&bk.drain[gm]));
-    mbar_wait(smem_u32(&bk.drain[gm]), 0, never, kDrainLimitNs);
-  } else {
-    // ---------------- compute warpgroups: one thread per tile row
-    const int g = (warp - kFirstComputeWarp) >> 2;
+    if (!ok && lane == 0) fail(bk, P.err);
+    // every MMA this warp issued completes before TMEM is released
+    umma_commit_warp(smem_u32(&bk.drain[c]));
+    mbar_wait(smem_u32(&bk.drain[c]), 0, never, kDrainLimitNs);
+  } else if (warp >= kFirstTWarp && warp < kFirstDWarp) {
+    // ---------------- transform warps: chunk k = 2L + h of x load L, into A
+    // buffer h.  A parity wait for phase p of an mbarrier is only sound when
+    // the waiter already knows phase p - 1 complete: earlier, the wait cannot
+    // tell p - 2 (same parity) from p and returns at once.  Every wait below
+    // follows that rule: on full_x / chunk_done / a_empty this half waited
+    // for the previous phase itself (a_empty[h] carries only this half's
+    // chunks).
+    const int h = (warp - kFirstTWarp) >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t a_base = tmem + (uint32_t)g * kWGC;
-    const uint32_t d_col = a_base + 2 * kACols;
-    // byte offsets of the row's 16-byte pieces p in a swizzled x tile
-    uint32_t xoff[8];
+    uint32_t xoff[8];  // byte offsets of the row's 16-byte pieces in a swizzled x tile
 #pragma unroll
     for (int p = 0; p < 8; ++p) xoff[p] = (uint32_t)row * kRowBytes + ((uint32_t)(p ^ (row & 7)) << 4);
-    const int my_units = (n - g + kWG - 1) / kWG;
-    const int my_chunks = kChunksPerSlice * my_units;
-
-    // transform of this warpgroup's chunk k: sum of squares and the x limbs
-    // into A buffer k % 2; returns the chunk's sum of squares
-    auto transform = [&](int k, float& tsq) -> bool {
-      const int r = k / kChunksPerSlice, c = k % kChunksPerSlice;
-      const int act = min(kWG, n - kWG * r);
-      // x stage of this chunk: rounds before r loaded kWG * kChunksPerSlice /
-      // kChunksPerStage stages each
-      const int i = r * kWG * (kChunksPerSlice / kChunksPerStage) + (c / kChunksPerStage) * act + g;
-      const int st = i % kXStages;
-      const uint32_t ph = (uint32_t)(i / kXStages) & 1u;
-      bool ok = mbar_wait(smem_u32(&bk.full_x[st]), ph, abort_flag, kWaitLimitNs);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) return false;
-      const uint32_t xt = smem_u32(x_smem(st)) + (uint32_t)(c % kChunksPerStage) * kXChunkBytes;
+    bool ok = true;
+    for (int L = 0; L < n_loads; ++L) {
+      const int k = kChunksPerStage * L + h;
+      const int st = L % kXStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.full_x[st]),
+                                             (uint32_t)(L / kXStages) & 1u, abort_flag,
+                                             kWaitLimitNs));
+      if (!ok) break;
+      const uint32_t xt = x_base + (uint32_t)st * kXBytes + (uint32_t)h * kXChunkBytes;
       uint32_t xw[32];
 #pragma unroll
       for (int p = 0; p < 8; ++p) {
         const uint4 v = lds128(xt + xoff[p]);
         xw[4 * p] = v.x; xw[4 * p + 1] = v.y; xw[4 * p + 2] = v.z; xw[4 * p + 3] = v.w;
       }
-      tsq = sq_tree64_f32x2(xw);
-      const uint32_t a_col = a_base + (uint32_t)(k & 1) * kACols;
+      // the row is in registers: this warp's half of the stage is released
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bk.empty_x[st]));
+      const float tsq = sq_tree64_f32x2(xw);
+      uint32_t lo[32];  // exact: x0; tf32x3: x[0:32] as fp32.  xw becomes x1 / x[32:64].
       if constexpr (kTf32) {
-        // x as fp32 (bf16 is exact in tf32), column c = chunk column c
-        uint32_t lo[32], hi[32];
+        uint32_t hi[32];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
           lo[2 * t] = xw[t] << 16;
@@ -720,114 +847,210 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
           hi[2 * t] = xw[16 + t] << 16;
           hi[2 * t + 1] = xw[16 + t] & 0xffff0000u;
         }
-        tmem_st32(lanes | a_col, lo);
-        tmem_st32(lanes | (a_col + 32), hi);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) xw[t] = hi[t];
       } else {
         // x0 = x rounded to the grid 2^(ex-5) with the bf16 magic constant
         // 1.5 * 2^(ex+2) (x + magic stays in one binade, so one bf16 rounding
         // puts x on the grid); x1 = x - x0 is exact.  Both are bf16, <= 8 bits.
         const uint32_t magic = bf16x2_split_magic(xw);
-        uint32_t w0[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
-          w0[t] = bf16x2_sub(bf16x2_fma(xw[t], kBf16x2One, magic), magic);
-          xw[t] = bf16x2_sub(xw[t], w0[t]);  // x1, in place
+          lo[t] = bf16x2_sub(bf16x2_fma(xw[t], kBf16x2One, magic), magic);
+          xw[t] = bf16x2_sub(xw[t], lo[t]);  // x1, in place
         }
-        // the stores complete in the background; tcgen05.wait::st comes
-        // before the A buffer is handed to the MMA warp
-        tmem_st32(lanes | a_col, w0);
-        tmem_st32(lanes | (a_col + 32), xw);
       }
-      if (c % kChunksPerStage == kChunksPerStage - 1) {  // both chunks of the stage read
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bk.empty_x[st]));
+      // sq slot k % kNumSq is free once the accumulate warps have read chunk
+      // k - kNumSq; A buffer h once the MMAs of chunk k - 2 are done
+      if (k >= kNumSq) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.chunk_done[k % kNumSq]),
+                                               (uint32_t)(k / kNumSq - 1) & 1u, abort_flag,
+                                               kWaitLimitNs));
+        if (!ok) break;
       }
-      return true;
-    };
-
-    float2 acc[kMix / 2];
-#pragma unroll
-    for (int j = 0; j < kMix / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-    float sqs = 0.0f, tsq_cur = 0.0f, tsq_next = 0.0f;
-    bool ok = my_chunks > 0 ? transform(0, tsq_cur) : true;
-    if (ok && my_chunks > 0) {
+      sq_buf[(k % kNumSq) * kTileM + row] = tsq;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bk.sq_full[k % kNumSq]));
+      if (k >= kNumA) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.a_empty[h]),
+                                               (uint32_t)(k / kNumA - 1) & 1u, abort_flag,
+                                               kWaitLimitNs));
+        if (!ok) break;
+      }
+      tc_fence_after();
+      const uint32_t a_col = tmem + (uint32_t)(k % kNumA) * kACols;
+      tmem_st32(lanes | a_col, lo);
+      tmem_st32(lanes | (a_col + 32), xw);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bk.a_ready[g]));
+      if (lane == 0) mbar_arrive(smem_u32(&bk.mma_ready[k % kNumD]));
     }
-    for (int k = 0; ok && k < my_chunks; ++k) {
-      if (k + 1 < my_chunks) {
-        ok = transform(k + 1, tsq_next);
-        if (!ok) break;
+    if (!ok) fail(bk, P.err);
+  } else if (warp >= kFirstDWarp) {
+    // ---------------- accumulate warps: first the second slice's W (when the
+    // CTA has one), which is not needed before the first unit is done; then
+    // chunk dots into slice totals
+    if (P.w_src != nullptr && n_sl >= 2) {
+      convert_slice(1, threadIdx.x - kFirstDWarp * 32, 4 * 32, false);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 4 * 32);
+      if (threadIdx.x == kFirstDWarp * 32)
+        for (int c = 0; c < kChunksPerSlice; ++c)
+          mbar_arrive(smem_u32(&bk.w_full[kChunksPerSlice + c]));
+    }
+    // A CTA with more than two slices reuses the slots: once these warps
+    // have read the last chunk of slice j - 2, every MMA of that slice is
+    // complete, and they fill slice j's slot (j % 2) before reading on.
+    auto refill = [&](int jn) {
+      const int slot = jn % kSlots;
+      if (P.w_src != nullptr) {
+        convert_slice(jn, threadIdx.x - kFirstDWarp * 32, 4 * 32, false);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 4 * 32);
+        if (threadIdx.x == kFirstDWarp * 32)
+          for (int c = 0; c < kChunksPerSlice; ++c)
+            mbar_arrive(smem_u32(&bk.w_full[slot * kChunksPerSlice + c]));
+      } else if constexpr (!kTf32) {
+        if (threadIdx.x == kFirstDWarp * 32)
+          for (int c = 0; c < kChunksPerSlice; ++c)
+            issue_w_load(slot, c, s_first + jn, l2_policy_evict_last());
       }
-      ok = mbar_wait(smem_u32(&bk.d_ready[g]), (uint32_t)k & 1u, abort_flag, kWaitLimitNs);
-      ok = __all_sync(0xffffffffu, ok);
+    };
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
+    const uint64_t keep = l2_policy_evict_last();  // the tail reads the partials next
+    float2 acc[kMix / 2];
+#pragma unroll
+    for (int j = 0; j < kMix / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+    float sqs = 0.0f;
+    bool ok = true;
+    for (int k = 0; k < n_chunks; ++k) {
+      // D of chunk k complete, and the chunk's sum of squares in its slot
+      bool got = mbar_wait(smem_u32(&bk.d_full[k % kNumD]), (uint32_t)(k / kNumD) & 1u, abort_flag,
+                           kWaitLimitNs);
+      got = got && mbar_wait(smem_u32(&bk.sq_full[k % kNumSq]), (uint32_t)(k / kNumSq) & 1u,
+                             abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, got);
       if (!ok) break;
       tc_fence_after();
-      // exact: D = [top | r1 | r2 | r3]; chunk dot = top + ((r1 + r2) + r3), in
-      // output pairs; all 96 columns in one TMEM round trip.  tf32x3: D's first
-      // 24 columns are the chunk dot.
-      uint32_t dv[kTf32 ? kMix : 4 * kMix];
+      const uint32_t d_col = tmem + kDCol0 + (uint32_t)(k % kNumD) * kDCols<kTf32>;
+      const float tsq = sq_buf[(k % kNumSq) * kTileM + row];
       if constexpr (kTf32) {
+        uint32_t dv[kMix];
         tmem_ld16(lanes | d_col, dv);
         tmem_ld8(lanes | (d_col + 16), dv + 16);
-      } else {
-        tmem_ld32(lanes | d_col, dv);
-        tmem_ld32(lanes | (d_col + 32), dv + 32);
-        tmem_ld32(lanes | (d_col + 64), dv + 64);
-      }
-      tmem_wait_ld();
-      // A(k+1) is written and D has been read: the MMAs of chunk k+1 may run
-      // while this chunk's dot is formed
-      if (k + 1 < my_chunks) {
-        tmem_wait_st();
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bk.a_ready[g]));
-      }
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
+          mbar_arrive(smem_u32(&bk.mma_ready[k % kNumD]));  // D buffer free for chunk k + 4
+        }
 #pragma unroll
-      for (int j = 0; j < kMix / 2; ++j) {
-        const float2 top = make_float2(__uint_as_float(dv[2 * j]), __uint_as_float(dv[2 * j + 1]));
-        if constexpr (kTf32) {
-          acc[j] = __fadd2_rn(acc[j], top);
-        } else {
-          const float2 u = make_float2(__uint_as_float(dv[kMix + 2 * j]), __uint_as_float(dv[kMix + 2 * j + 1]));
-          const float2 v = make_float2(__uint_as_float(dv[2 * kMix + 2 * j]), __uint_as_float(dv[2 * kMix + 2 * j + 1]));
-          const float2 w = make_float2(__uint_as_float(dv[3 * kMix + 2 * j]), __uint_as_float(dv[3 * kMix + 2 * j + 1]));
-          acc[j] = __fadd2_rn(acc[j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
+        for (int j = 0; j < kMix / 2; ++j)
+          acc[j] = __fadd2_rn(acc[j], make_float2(__uint_as_float(dv[2 * j]),
+                                                  __uint_as_float(dv[2 * j + 1])));
+      } else {
+        // D = [top | r1 | r2 | r3] (24 columns each); chunk dot = top + ((r1 +
+        // r2) + r3).  Outputs 0..15 first, then 16..23 (two TMEM round trips
+        // keep the registers within the 512-thread budget).
+        {
+          uint32_t dv[4][16];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) tmem_ld16(lanes | (d_col + 24 * g), dv[g]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float2 top = make_float2(__uint_as_float(dv[0][2 * j]), __uint_as_float(dv[0][2 * j + 1]));
+            const float2 u = make_float2(__uint_as_float(dv[1][2 * j]), __uint_as_float(dv[1][2 * j + 1]));
+            const float2 v = make_float2(__uint_as_float(dv[2][2 * j]), __uint_as_float(dv[2][2 * j + 1]));
+            const float2 w = make_float2(__uint_as_float(dv[3][2 * j]), __uint_as_float(dv[3][2 * j + 1]));
+            acc[j] = __fadd2_rn(acc[j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
+          }
+        }
+        {
+          uint32_t dv[4][8];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) tmem_ld8(lanes | (d_col + 24 * g + 16), dv[g]);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
+            mbar_arrive(smem_u32(&bk.mma_ready[k % kNumD]));  // D buffer free for chunk k + 4
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 top = make_float2(__uint_as_float(dv[0][2 * j]), __uint_as_float(dv[0][2 * j + 1]));
+            const float2 u = make_float2(__uint_as_float(dv[1][2 * j]), __uint_as_float(dv[1][2 * j + 1]));
+            const float2 v = make_float2(__uint_as_float(dv[2][2 * j]), __uint_as_float(dv[2][2 * j + 1]));
+            const float2 w = make_float2(__uint_as_float(dv[3][2 * j]), __uint_as_float(dv[3][2 * j + 1]));
+            acc[8 + j] = __fadd2_rn(acc[8 + j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
+          }
         }
       }
-      sqs = __fadd_rn(sqs, tsq_cur);
-      tsq_cur = tsq_next;
+      sqs = __fadd_rn(sqs, tsq);
       if (k % kChunksPerSlice == kChunksPerSlice - 1) {
-        const int64_t unit = u_begin + kWG * (k / kChunksPerSlice) + g;
-        const int tile = unit_tile(unit), s = unit_slice(unit);
-        // the reduce kernel reads the partials next: keep them in L2 while x
-        // streams through it with evict_first
-        float* p = part + (int64_t)s * kPartStride * Mpad + (int64_t)tile * kTileM + row;
-        const uint64_t keep = l2_policy_evict_last();
+        const int i = k / kChunksPerSlice;
+        float* p = P.part + part_index(unit_tile(i) * kTileM + row, unit_slice(i), 0, P.n_slices);
 #pragma unroll
         for (int j = 0; j < kMix / 2; ++j) {
-          stg_f32_hint(p + (int64_t)(2 * j) * Mpad, acc[j].x, keep);
-          stg_f32_hint(p + (int64_t)(2 * j + 1) * Mpad, acc[j].y, keep);
+          stg_f32_hint(p + 8 * (2 * j), acc[j].x, keep);
+          stg_f32_hint(p + 8 * (2 * j + 1), acc[j].y, keep);
           acc[j] = make_float2(0.0f, 0.0f);
         }
-        stg_f32_hint(p + (int64_t)kMix * Mpad, sqs, keep);
+        stg_f32_hint(p + 8 * kMix, sqs, keep);
         sqs = 0.0f;
+        // the last unit of slice j done: slice j + 2 (if any) may take its slot
+        const int j = unit_slice(i) - s_first;
+        if (j + kSlots < n_sl && (i == n - 1 || unit_slice(i + 1) != unit_slice(i)))
+          refill(j + kSlots);
       }
     }
-    if (!ok) fail(bk, err);
+    if (!ok) fail(bk, P.err);
+    if constexpr (!kTf32) {
+      // the TMA loads of prepacked limbs complete before the CTA can exit
+      if (P.w_src == nullptr && threadIdx.x == kFirstDWarp * 32)
+        for (int j = max(0, n_sl - kSlots); j < n_sl; ++j)
+          for (int c = 0; c < kChunksPerSlice; ++c)
+            mbar_wait(smem_u32(&bk.w_full[(j % kSlots) * kChunksPerSlice + c]),
+                      (uint32_t)(j / kSlots) & 1u, never, kDrainLimitNs);
+    }
   }
 
-  // ---- teardown: every role has finished (or given up); free TMEM
+  // ---- every role has finished (or given up); TMEM is no longer needed
   tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
+  cta_barrier();
+  if (warp == kMmaWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (P.tail == 0) return;
+
+  // ---- tail: once every CTA's partials are stored (grid barrier) this CTA
+  // adds the slices of its rows in slice order and runs the epilogue; the x
+  // and W buffers are idle now and hold the tail's copies
+  if (threadIdx.x == 0 &&
+      !grid_barrier(P.gbar_count, P.gbar_gen, (uint32_t)G, kWaitLimitNs))
+    record_device_error(P.err, kDevWaitTimeout);
+  cta_barrier();
+  tc_tail(P, smem, bk.tail_bar, never, b, G);
 }
+
+// The tail alone (HCMIX_PATH_TC_STAGED): the same reduce and epilogue as the
+// fused kernel's, as a kernel of its own after the contraction.
+__global__ void __launch_bounds__(kTailThreads, 1) hcmix_tc_tail_kernel(const __grid_constant__ TcParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tb = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  uint64_t* tbar = reinterpret_cast<uint64_t*>(tb + kTailBytes);
+  __shared__ int never;
+  if (threadIdx.x == 0) never = 0;  // ordered before any wait by the barrier inside the tail
+  tc_tail(P, tb, tbar, &never, blockIdx.x, gridDim.x);
+}
+constexpr size_t kTailKernelSmem = kTailBytes + kTailSlots * 8 + 128;
 
 // ---------------------------------------------------------------- host side
 
@@ -885,100 +1108,108 @@ inline bool make_map_bf16_3d_chunks(CUtensorMap* map, const void* base, uint64_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 4-D view of the tf32x3 parts[2][24][K] (fp32) as [part][K / 32 halves]
-// [24 rows][32]: one box is both parts of two consecutive 32-column halves
-// (one chunk) with 32 rows, stored in shared memory as [part][half][32 rows x
-// 128 B] with the 128-byte swizzle; rows 24..31 lie past the tensor and are
-// filled with zeros.
-inline bool make_map_tf32_parts(CUtensorMap* map, const float* parts, uint64_t K) {
-  EncodeTiledFn fn = encode_tiled_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[4] = {32, (cuuint64_t)kMix, K / 32, 2};
-  const cuuint64_t strides[3] = {K * 4, 128, (cuuint64_t)kMix * K * 4};
-  const cuuint32_t box[4] = {32, kTf32Rows, 2, 2};
-  const cuuint32_t elem[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(parts), dims, strides,
-            box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// The tail kernel of the staged path: the same CTA count as the contraction.
+inline hcmix_status launch_tail(const TcParams& P, int64_t grid, cudaStream_t stream) {
+  if (cudaFuncSetAttribute(hcmix_tc_tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kTailKernelSmem) != cudaSuccess)
+    return HCMIX_ERR_CUDA;
+  hcmix_tc_tail_kernel<<<(unsigned)grid, kTailThreads, kTailKernelSmem, stream>>>(P);
+  return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
 }
 
 template <bool kTf32>
-hcmix_status launch_main(const CUtensorMap& mx, const CUtensorMap& mw, int64_t M, int64_t K,
-                         float* part, int Mpad, uint32_t* err, const float* w_src,
-                         int64_t w_stride, bool dependent, cudaStream_t stream) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return HCMIX_ERR_CUDA;
-  const int64_t n_tiles = (M + kTileM - 1) / kTileM;
-  const int64_t n_units = n_tiles * (K / kSlice);
-  const int64_t grid = n_units < sms ? n_units : sms;
+hcmix_status launch_main(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& P,
+                         int64_t grid, cudaStream_t stream) {
   if (cudaFuncSetAttribute(hcmix_tc_kernel<kTf32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes<kTf32>) != cudaSuccess)
     return HCMIX_ERR_CUDA;
-  // launched as a programmatic dependent of the pack kernel: x streams while
-  // W is being packed; the W producer waits for the pack grid
+  // cooperative: every CTA is resident at once, which the grid barrier before
+  // the tail relies on (one CTA per SM, grid <= #SMs)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes<kTf32>;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = dependent ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, hcmix_tc_kernel<kTf32>, mx, mw, (int)n_tiles, Mpad, n_units, part,
-                         err, w_src, w_stride) != cudaSuccess)
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, hcmix_tc_kernel<kTf32>, mx, mw, P) != cudaSuccess)
     return HCMIX_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HCMIX_OK : HCMIX_ERR_CUDA;
 }
 
 }  // namespace tc
 
-// Packs W (exact limbs, or the tf32x3 big / small parts), then runs the
-// tensor-core contraction into `part`.  `packed` is the workspace area of
-// 4 * 24 * K * 2 bytes (= 2 * 24 * K * 4) that holds the packed W.  With W
-// null (exact mode only), `packed` already holds limbs written by
-// hcmix_pack_limbs_kernel and nothing is packed.
+// What the tensor-core kernel does after its contraction.
+struct TcTail {
+  int tail;  // 0: partials only; 1: + mix / sq; 2: + epilogue
+  float inv_k;
+  const float* hc_scale;
+  const float* hc_base;
+  int iters;
+  float rms_eps, hc_eps;
+  float *pre, *post, *comb, *mix_out, *sq_out;
+};
+
+// The tensor-core path in one launch: contraction into `part`, then the tail.
+// W given: converted inside the kernel (exact limbs, or the tf32x3 big /
+// small parts).  W null (exact mode only): `packed` holds limbs written by
+// hcmix_pack_limbs_kernel, loaded with TMA.  `header` is the workspace header
+// (error word at 0, grid-barrier words at 64 and 128 bytes).  `staged`: the
+// tail runs as a second kernel instead (HCMIX_PATH_TC_STAGED).
 inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* W,
-                              int64_t w_stride, int64_t M, int64_t K, void* packed,
-                              float* part, int Mpad, uint32_t* err, cudaStream_t stream,
-                              bool tf32x3) {
-  if (W == nullptr && tf32x3) return HCMIX_ERR_INVALID_ARG;  // prepacked W: exact limbs only
-  CUtensorMap mx, mw;
-  if (!tc::make_map_bf16_3d_chunks(&mx, x, (uint64_t)K, (uint64_t)M, (uint64_t)x_stride * 2,
-                                    tc::kTileM, tc::kChunksPerStage))
-    return HCMIX_ERR_CUDA;
-  if (tf32x3) {
-    float* parts = static_cast<float*>(packed);
-    const int64_t n4 = kMix * (K / 4);
-    tc::hcmix_pack_tf32_kernel<<<(unsigned)((n4 + tc::kPackThreads - 1) / tc::kPackThreads),
-                                 tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K, parts);
-    if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
-    if (!tc::make_map_tf32_parts(&mw, parts, (uint64_t)K)) return HCMIX_ERR_CUDA;
-    return tc::launch_main<true>(mx, mw, M, K, part, Mpad, err, nullptr, 0, true, stream);
-  }
-  uint16_t* limbs = static_cast<uint16_t*>(packed);
-  if (!tc::make_map_bf16_2d(&mw, limbs, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
-                            tc::kLimbRows))
-    return HCMIX_ERR_CUDA;
-  if (W == nullptr)  // limbs packed ahead of the call
-    return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, nullptr, 0, false, stream);
+                              int64_t w_stride, int64_t M, int64_t K, const void* packed,
+                              float* part, int Mpad, uint32_t* header, const TcTail& t,
+                              cudaStream_t stream, bool tf32x3, bool staged = false) {
+  if (W == nullptr && (tf32x3 || packed == nullptr)) return HCMIX_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return HCMIX_ERR_CUDA;
-  const int64_t n_units = (M + tc::kTileM - 1) / tc::kTileM * (K / kSlice);
-  if (n_units <= sms)  // one unit per CTA: each CTA splits its own slice of W
-    return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, W, w_stride, false, stream);
-  const int nch = (int)(K / kChunk);
-  const int pack_blocks = (kMix * nch + tc::kPackTasksPerBlock - 1) / tc::kPackTasksPerBlock;
-  tc::hcmix_pack_limbs_kernel<<<pack_blocks, tc::kPackThreads, 0, stream>>>(W, w_stride, (int)K,
-                                                                           limbs);
-  if (cudaGetLastError() != cudaSuccess) return HCMIX_ERR_CUDA;
-  return tc::launch_main<false>(mx, mw, M, K, part, Mpad, err, nullptr, 0, true, stream);
+  CUtensorMap mx, mw;
+  if (!tc::make_map_bf16_3d_chunks(&mx, x, (uint64_t)K, (uint64_t)M, (uint64_t)x_stride * 2,
+                                    tc::kTileM, tc::kChunksPerStage))
+    return HCMIX_ERR_CUDA;
+  if (W == nullptr) {
+    if (!tc::make_map_bf16_2d(&mw, packed, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
+                              tc::kLimbRows))
+      return HCMIX_ERR_CUDA;
+  } else {
+    mw = mx;  // not used: W is converted inside the kernel
+  }
+  tc::TcParams P = {};
+  P.n_tiles = (int)((M + tc::kTileM - 1) / tc::kTileM);
+  P.n_slices = (int)(K / kSlice);
+  P.M = (int)M;
+  P.Mpad = Mpad;
+  P.n_units = (int64_t)P.n_tiles * P.n_slices;
+  P.part = part;
+  P.err = header;
+  P.gbar_count = header + 16;
+  P.gbar_gen = header + 32;
+  P.w_src = W;
+  P.w_stride = w_stride;
+  P.tail = t.tail;
+  P.inv_k = t.inv_k;
+  P.hc_scale = t.hc_scale;
+  P.hc_base = t.hc_base;
+  P.iters = t.iters;
+  P.rms_eps = t.rms_eps;
+  P.hc_eps = t.hc_eps;
+  P.pre = t.pre;
+  P.post = t.post;
+  P.comb = t.comb;
+  P.mix_out = t.mix_out;
+  P.sq_out = t.sq_out;
+  const int64_t grid = P.n_units < sms ? P.n_units : sms;
+  if (staged) P.tail = 0;
+  const hcmix_status st = tf32x3 ? tc::launch_main<true>(mx, mw, P, grid, stream)
+                                 : tc::launch_main<false>(mx, mw, P, grid, stream);
+  if (st != HCMIX_OK || !staged || t.tail == 0) return st;
+  P.tail = t.tail;
+  return tc::launch_tail(P, grid, stream);
 }
 
 // W[24, K] fp32 -> limbs[4][24][K] bf16, the tensor-core kernel's B operand.

@@ -80,13 +80,21 @@ typedef enum {
  * Per chunk its error is at most (2^-19 + 2^-21) * sum |x| |W| over the chunk
  * (16 fp32 accumulations and the tf32 truncation of the small part), and its
  * tests hold each output within 2^-18 * sum_k |x[m,k]| |W[j,k]| of the exact
- * result; sq is bit-identical to the other paths.  AUTO never selects it. */
+ * result; sq is bit-identical to the other paths.  AUTO never selects it.
+ *
+ * HCMIX_PATH_TC runs the whole call in one launch: the contraction stores its
+ * per-slice totals in the workspace, and the same kernel then adds them in
+ * slice order and runs the epilogue after a grid-wide barrier.
+ * HCMIX_PATH_TC_STAGED runs the same contraction but leaves the ordered reduce
+ * and the epilogue to a second kernel, as the page's stock engine does; its
+ * results are bit-identical to HCMIX_PATH_TC's (an A/B of the fused tail). */
 typedef enum {
   HCMIX_PATH_AUTO = 0,
   HCMIX_PATH_SIMT = 1,       /* CUDA-core split-K kernel (stock layout) */
   HCMIX_PATH_TC = 2,         /* tcgen05 tensor-core split-K kernel */
   HCMIX_PATH_SIMT_FULLK = 3, /* CUDA-core full-K kernel (the page's fused design) */
-  HCMIX_PATH_TC_TF32X3 = 4   /* tensor-core split-K kernel with the page's tf32x3 chunk dots */
+  HCMIX_PATH_TC_TF32X3 = 4,  /* tensor-core split-K kernel with the page's tf32x3 chunk dots */
+  HCMIX_PATH_TC_STAGED = 5   /* HCMIX_PATH_TC's contraction, then the separate reduce kernel */
 } hcmix_path;
 
 /* Bytes of device workspace that hc_mix_stats / hc_mix_fused need for M rows.

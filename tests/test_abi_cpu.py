@@ -36,11 +36,10 @@ def test_exports_every_declared_symbol(L):
 def test_workspace_bytes(L):
     K = 20480
     n = binding.workspace_bytes(4096, K)
-    limbs = 4 * 24 * K * 2
     parts = 80 * 25 * 4096 * 4
-    assert n == 256 + limbs + parts
-    assert binding.workspace_bytes(1, K) == 256 + limbs + 80 * 25 * 128 * 4
-    assert binding.workspace_bytes(0, K) == 256 + limbs
+    assert n == 256 + parts  # header (error word, grid-barrier words) + partials
+    assert binding.workspace_bytes(1, K) == 256 + 80 * 25 * 128 * 4
+    assert binding.workspace_bytes(0, K) == 256
     assert binding.workspace_bytes(16, 20481) == 0     # K not a multiple of 256
     assert binding.workspace_bytes(16, K, mix=16) == 0  # mix != 24
     assert binding.workspace_bytes(-1, K) == 0
@@ -117,7 +116,7 @@ def test_host_validation_rejects_before_launch(L):
     assert _stats(L, wkb=1024) == 4          # workspace too small
     assert _stats(L, x=None) == 1
     assert _stats(L, path=7) == 1
-    assert _stats(L, path=5) == 1            # one past the last declared path
+    assert _stats(L, path=6) == 1            # one past the last declared path
     assert _stats(L, path=-1) == 1
     assert _stats(L, mo=None) == 1
     assert _stats(L, M=0, x=None, W=None, wk=None) == 0  # empty: nothing to do

@@ -18,7 +18,7 @@ from pin_inputs import rms_pin_closed_form, rms_pin_inputs
 pytestmark = pytest.mark.gpu
 
 THREADS = os.cpu_count() or 1
-PATHS = ("simt", "tc", "simt_fullk")
+PATHS = ("simt", "tc", "simt_fullk", "tc_staged")
 
 
 def dev_x(x):
@@ -131,6 +131,15 @@ def test_rms_eps_placement_inputs(path, case):
     assert np.max(np.abs(got[0][0] - p)) <= 1e-6
     assert np.max(np.abs(got[1][0] - q)) <= 1e-6
     assert np.max(np.abs(got[2][0] - C)) <= 1e-5
+
+
+@pytest.mark.parametrize("M", [5, 130])
+def test_long_k_more_slices_than_slots(path, M):
+    """K = 131072 (512 slices): with 152 CTAs each CTA covers three or more
+    slices, so the tensor-core kernel refills its two W slots while it runs."""
+    K = 131072
+    check_all(hi.make_x(M, K=K), hi.make_w(K=K), hi.make_scale(), hi.make_base(), path,
+              f"M={M} K={K}")
 
 
 def test_integer_inputs_bit_exact(path):
@@ -277,6 +286,29 @@ def test_fullk_bit_identical_to_split_k(M, K):
         assert np.array_equal(u.view(np.uint32), v.view(np.uint32)), f"{name} differs"
 
 
+@pytest.mark.parametrize("case", ["m4096", "m512_outliers", "decode"])
+def test_fused_tail_bit_identical_to_separate_reduce(case):
+    """The tensor-core path's in-kernel tail (grid barrier, slice-ordered reduce
+    and epilogue in the contraction kernel) against the same contraction
+    followed by the separate reduce kernel: the same values are added in the
+    same order, so every output bit agrees."""
+    for p in ("tc", "tc_staged"):
+        if not path_available(p):
+            pytest.fail(f"kernel path {p} is not available in this library")
+    W, sc, bs = hi.make_w(), hi.make_scale(), hi.make_base()
+    if case == "decode":
+        xs = [np.ascontiguousarray(hi.make_x(256)[:M]) for M in (1, 4, 16, 64, 128, 256)]
+    else:
+        xs = [hi.make_x(4096)] if case == "m4096" else [hi.make_x(512, outliers=True)]
+    for x in xs:
+        xt = dev_x(x)
+        a = run(x, W, sc, bs, "tc", x_dev=xt)
+        b = run(x, W, sc, bs, "tc_staged", x_dev=xt)
+        for name, u, v in zip(("pre", "post", "comb", "mix", "sq"), a, b):
+            assert np.array_equal(u.view(np.uint32), v.view(np.uint32)), \
+                f"{case} M={x.shape[0]}: {name} differs"
+
+
 # ---- tf32x3 mode: the page's chunk arithmetic (big = tf32 RNA of W, small =
 # W - big, dot(x, small) then dot(x, big) per chunk as tf32 MMAs).  The tensor
 # core rounds inside every chunk dot, so the mode is held to a bound derived
@@ -371,17 +403,17 @@ def test_tf32x3_is_not_auto():
     assert binding.hc_mix_auto_path(1) != "tc_tf32x3"
 
 
-@pytest.mark.parametrize("M", [1, 130, 4096])
-def test_fused_packed_matches_fused(M):
+@pytest.mark.parametrize("M,K", [(1, 20480), (130, 20480), (4096, 20480), (130, 131072)])
+def test_fused_packed_matches_fused(M, K):
     """W packed once gives the tensor-core path's results bit for bit, and a
     repacked buffer follows a new W."""
     if not path_available("tc"):
         pytest.fail("kernel path tc is not available in this library")
-    x = dev_x(hi.make_x(M, outliers=True))
+    x = dev_x(hi.make_x(M, K=K, outliers=True))
     sc, bs = dev(hi.make_scale()), dev(hi.make_base())
     packed = None
     for seed in (1, 7):
-        W = dev(hi.make_w(seed=seed))
+        W = dev(hi.make_w(K=K, seed=seed))
         packed = binding.pack_w(W, packed=packed)
         a = binding.hc_mix_fused(x, W, sc, bs, want_stats=True, path="tc")
         b = binding.hc_mix_fused_packed(x, packed, sc, bs, want_stats=True)
