@@ -92,18 +92,29 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until phase `parity` of `bar` completes.  Gives up (returns false)
-// after `limit_ns` of wall clock or when *abort becomes non-zero.  It polls
-// with short sleeps rather than suspending in try_wait: a thread suspended
-// there resumed some hundreds of nanoseconds after the phase completed, and
-// the hand-offs of the pipeline are shorter than that.
+// after `limit_ns` of wall clock or when *abort becomes non-zero.  Between
+// tests the thread sleeps in try_wait (the hardware wakes it when the phase
+// completes or after its own time limit), so a waiting warp takes no issue
+// slots from the warps that share its sub-partition.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile int* abort, uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
-    __nanosleep(32);
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 3u) == 0) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > limit_ns) return false;
     }
@@ -254,7 +265,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
       : "memory");
 }
 
-// Warp-collective: thread i reads 8 / 16 / 32 columns of its lane.
+// Warp-collective: thread i reads 4 / 8 / 16 / 32 columns of its lane.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* v) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* v) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"

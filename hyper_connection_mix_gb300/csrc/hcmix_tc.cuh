@@ -8,35 +8,42 @@
 // workload sizes (more only when K exceeds 152 slices), and the W operand of
 // those slices stays in shared memory for the whole range.
 //
-// One CTA = 16 warps with fixed roles, each role a stage of a pipeline over
-// the CTA's 64-column chunks (k = 0, 1, ... in unit order, four per unit):
-//   * warp 0 (one lane) loads x with TMA, two chunks of a tile (32 KB, 128-byte
-//     swizzle) per load, into a 3-stage ring;
-//   * the eight transform warps (warps 4..11, two per TMEM lane quadrant;
-//     warp 4 + 4h + q takes the chunks k with k % 2 == h for tile rows 32q..)
-//     read their row of the chunk, sum its squares by the page's fixed tree,
-//     split x into the limbs x0 (grid-aligned) and x1 = x - x0, and store both
-//     into TMEM A buffer k % 4 (x as fp32 in tf32x3 mode); the chunk's sum of
-//     squares goes to a shared-memory slot beside it;
-//   * warp 1 issues the chunk's 8 MMAs (M=128, N=96, K=16, A in TMEM, B in
-//     shared memory) into TMEM D buffer k % 2:  B rows [0 | w0 | w1 | w2]
-//     against x1, then [w0 | w1 | w2 | w3] against x0, so that
+// One CTA = 20 warps with fixed roles, each role a stage of a pipeline over
+// the CTA's 64-column chunks (k = 0, 1, ... in unit order, four per unit).
+// Warp w runs on sub-partition w % 4 and may touch TMEM lanes 32 (w % 4)..:
+//   * warps 0..2, the MMA issuers: warp t issues the chunks with k % 3 == t,
+//     8 MMAs each (M=128, N=96, K=16, A in TMEM, B in shared memory) into
+//     TMEM D buffer t: B rows [0 | w0 | w1 | w2] against x1, then [w0 | w1 |
+//     w2 | w3] against x0, so that
 //       D = [x0.w0 | x0.w1 + x1.w0 | x0.w2 + x1.w1 | x0.w3 + x1.w2]
 //     (the first 24 columns exact; x1.w3 ~ 2^-34 relative is dropped);
-//   * the four accumulate warps (warps 12..15, one per quadrant) read D, form
-//     the chunk dot fl32(top + ((r1 + r2) + r3)), add it into the slice total
-//     (chunks in order, from zero), add the chunk's sum of squares likewise,
-//     and at the end of each unit store its 24 + 1 slice totals per row to the
-//     workspace partials;
+//   * warp 3 (one lane), the x producer: TMA loads of two chunks of a tile
+//     (32 KB, 128-byte swizzle) into a 3-stage ring, the first ones during
+//     set-up.  It issues nothing else, so no other role's shared-memory
+//     accesses queue behind its copies;
+//   * warps 4..11, the transform warps, two halves of four (one per
+//     quadrant): half h takes the chunks with k % 2 == h.  Each thread reads
+//     its row of the chunk from the x stage, sums its squares by the page's
+//     fixed tree, splits x into the limbs x0 (grid-aligned) and x1 = x - x0
+//     and stores both into TMEM A buffer k % 3 (x as fp32 in tf32x3 mode);
+//     the chunk's sum of squares goes to a shared-memory slot;
+//   * warps 12..19, the accumulate warps, two output groups of four: warp
+//     12 + 4 e + q reads outputs 12 e .. 12 e + 11 of the rows of quadrant q
+//     (4 x 12 D columns, one TMEM round trip), forms the chunk dots
+//     fl32(top + ((r1 + r2) + r3)), adds them into the slice totals (chunks
+//     in order, from zero) and stores them at the end of each unit to the
+//     workspace partials; group 0 does the same for the sums of squares;
 //   * the W operand: every CTA converts the fp32 W of its first two slices
 //     into the exact bf16 limbs (or the tf32x3 big / small parts) in shared
-//     memory during set-up, with all 512 threads (no separate pack kernel);
-//     warp 2 refills a slot when a CTA covers more slices, or TMA-loads limbs
-//     that hc_mix_pack_w wrote ahead of time.
-// A buffer k % 4 is handed back when the accumulate warps have read chunk k
-// (which is after its MMAs have completed), D buffer k % 2 likewise, so the
-// transform warps run up to three chunks ahead of the MMAs and the MMAs of
-// chunk k + 1 execute while chunk k is being read.
+//     memory during set-up (no separate pack kernel); the accumulate warps
+//     refill a slot when the CTA covers more slices, or TMA-load limbs that
+//     hc_mix_pack_w wrote ahead of time.
+// The A and D rings are three deep, so that neither hand-off loop (A buffer:
+// written, MMAs issued and completed, rewritten; D buffer: MMAs completed,
+// read, next MMAs issued) spans fewer than three chunks.  Every mbarrier wait
+// is by a waiter that has seen the barrier's previous phase, as a parity wait
+// needs: A buffer k % 3 is freed on a_empty[k % 3][k % 2], which only the
+// other transform half (the writer of chunk k + 3) waits on.
 //
 // Tail (same kernel): once every CTA has stored its partials (a grid-wide
 // barrier; the launch is cooperative, so every CTA is resident), CTA b adds
@@ -69,18 +76,23 @@ namespace tc {
 
 constexpr int kXStages = 3;        // x stages in flight
 constexpr int kChunksPerStage = 2;  // an x stage holds two chunks of a tile (one 32 KB load)
-constexpr int kNumA = 2;   // TMEM A buffers: A buffer h belongs to transform half h (chunks k % 2 == h)
-constexpr int kNumD = 4;   // TMEM D buffers: D buffer g belongs to MMA issuer g (chunks k % 4 == g)
+constexpr int kNumA = 3;   // TMEM A buffers: chunk k uses A buffer k % 3
+constexpr int kNumD = 3;   // TMEM D buffers: chunk k uses D buffer k % 3
 constexpr int kNumSq = 8;  // sum-of-squares slots (shared memory)
 constexpr int kSlots = 2;  // W slots: a CTA's consecutive slices alternate between them
 constexpr int kWBufs = kSlots * kChunksPerSlice;
-constexpr int kWarps = 17;
-constexpr int kThreads = kWarps * 32;
-constexpr int kXWarp = 0, kMmaWarp0 = 1;
-constexpr int kNumMma = 4;  // MMA-issuing warps 1..4: chunk k (= chunk c of its unit) to warp 1 + c
-constexpr int kFirstTWarp = 5;   // transform warps 5..12
+constexpr int kMmaWarp0 = 0, kTmemWarp = 1;
+constexpr int kNumMma = 3;  // MMA-issuing warps 0..2: chunk k to warp k % 3 (its A and D buffers)
+constexpr int kXWarp = 3;   // the x producer (one lane)
+constexpr int kFirstTWarp = 4;   // transform warps 4..11
 constexpr int kNumTWarps = 8;
-constexpr int kFirstDWarp = 13;  // accumulate warps 13..16
+constexpr int kFirstDWarp = 12;  // accumulate warps 12..19: warp 12 + 4 e + q, quadrant q, outputs 12 e..
+constexpr int kNumDWarps = 8;
+constexpr int kFirstWorkWarp = 4;  // transform and accumulate warps: kFirstWorkWarp ..
+constexpr int kWarps = kFirstWorkWarp + kNumTWarps + kNumDWarps;
+constexpr int kThreads = kWarps * 32;
+// registers per thread: the register file of a sub-partition (16K) over its warps
+constexpr int kMaxRegs = (16384 / (((kWarps + 3) / 4) * 32)) / 8 * 8;
 constexpr int kTileM = 128;
 constexpr uint32_t kRowBytes = 128;                           // 64 bf16 per smem row
 constexpr uint32_t kXChunkBytes = kTileM * kRowBytes;         // one chunk of a tile
@@ -130,8 +142,8 @@ constexpr size_t kSmemBytes = kBkOff<kTf32> + 1024 + 1024;  // bookkeeping + bas
 struct Bookkeeping {
   uint64_t full_x[kXStages];
   uint64_t empty_x[kXStages];
-  uint64_t a_empty[kNumA];
-  uint64_t mma_ready[kNumD];  // A(k) written (4 transform warps) and D(k % 4) read (4 accumulate warps)
+  uint64_t a_empty[kNumA * 2];  // [k % 3 * 2 + k % 2]: the MMAs of chunk k are done
+  uint64_t mma_ready[kNumMma];  // chunk k (issuer k % 3): A(k) written and D(k - 3) read
   uint64_t sq_full[kNumSq];
   uint64_t d_full[kNumD];
   uint64_t chunk_done[kNumSq];
@@ -150,11 +162,16 @@ static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of o
 static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynamic shared memory");
 static_assert(Mode<false>::kBBytes % 1024 == 0 && Mode<true>::kBlockBytes % 1024 == 0,
               "W buffers keep the 1 KB swizzle atoms aligned");
-static_assert(kNumTWarps == 2 * 4 && kFirstDWarp == kFirstTWarp + kNumTWarps &&
-                  kFirstDWarp + 4 == kWarps, "warp roles");
-static_assert(kNumMma == kNumD && kNumMma == kChunksPerSlice && kFirstTWarp == 1 + kNumMma &&
-                  kNumA == 2, "issuer g owns D buffer g and W buffers (slot, g); A buffer h "
-                              "belongs to transform half h");
+static_assert(kNumTWarps == 2 * 4 && kFirstTWarp % 4 == 0 && kFirstDWarp % 4 == 0 &&
+                  kFirstTWarp >= kFirstWorkWarp && kFirstDWarp >= kFirstWorkWarp &&
+                  kFirstTWarp + kNumTWarps <= kWarps && kFirstDWarp + kNumDWarps <= kWarps &&
+                  (kFirstTWarp + kNumTWarps <= kFirstDWarp || kFirstDWarp + kNumDWarps <= kFirstTWarp),
+              "warp roles");
+static_assert(kNumMma == 3 && kNumA == 3 && kNumD == 3 && kNumTWarps == 8 && kNumDWarps == 8 &&
+                  kXWarp < kFirstWorkWarp && kMmaWarp0 + kNumMma <= kFirstWorkWarp &&
+                  (kXWarp < kMmaWarp0 || kXWarp >= kMmaWarp0 + kNumMma),
+              "issuer k % 3 owns A and D buffer k % 3; the transform warps are two halves, the "
+              "accumulate warps two output groups");
 
 // Parameters of one launch (passed by value as a __grid_constant__).
 struct TcParams {
@@ -506,6 +523,8 @@ constexpr size_t kTailTotOff = (size_t)kTailSlots * kTailSlotBytes;
 constexpr size_t kTailParOff = kTailTotOff + (size_t)kPartStride * (kReduceRows + 1) * 4;
 constexpr size_t kTailBytes = (kTailParOff + 32 * 4 + 15) / 16 * 16;  // shared memory the tail uses
 constexpr int kTailThreads = 512;
+// the tail reuses the x / W buffers; the bookkeeping (its barriers) lies past them
+static_assert(kTailBytes <= kBkOff<false> && kTailBytes <= kBkOff<true>, "tail shared memory");
 
 // The tail of a call for CTA b of G: the octs [b n / G, (b + 1) n / G) of the
 // n = ceil(M / 8) octs.  Each half of the CTA (256 threads) takes every other
@@ -594,7 +613,7 @@ __device__ __forceinline__ void tc_tail(const TcParams& P, uint8_t* tb, uint64_t
 // ---------------------------------------------------------------- the kernel
 
 template <bool kTf32>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(kMaxRegs)
 hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ TcParams P) {
   using namespace sm100;
@@ -620,8 +639,10 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     return w_base + (uint32_t)(slot * kChunksPerSlice + c) * MD::kBBytes;
   };
   // unit i of this CTA: tile (u % n_tiles) of slice (u / n_tiles), u = u_begin + i
-  auto unit_tile = [&](int i) { return (int)((u_begin + i) % P.n_tiles); };
-  auto unit_slice = [&](int i) { return (int)((u_begin + i) / P.n_tiles); };
+  // (32-bit arithmetic from the CTA's first unit: i < n, and n_tiles fits)
+  const int tile0 = (int)(u_begin % P.n_tiles);
+  auto unit_tile = [&](int i) { return (tile0 + i) % P.n_tiles; };
+  auto unit_slice = [&](int i) { return s_first + (tile0 + i) / P.n_tiles; };
 
   // x load L fills stage L % kXStages with chunks 2L and 2L + 1 (unit L / 2)
   auto issue_x_load = [&](int L, uint64_t pol) {
@@ -646,82 +667,89 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     constexpr int kTasks = kMix * kChunksPerSlice;  // (output, chunk) pairs, 16 lanes each
     const int groups = nthreads / 16, sub = tid & 15;
     constexpr int kMaxRounds = 12;  // 96 tasks over at least 8 groups
-    float4 wv[kMaxRounds];
+    constexpr int kBatch = 6;       // rounds whose loads are in flight together
 #pragma unroll
-    for (int q = 0; q < kMaxRounds; ++q) {
-      const int task = q * groups + (tid >> 4);
-      wv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (task < kTasks)
-        wv[q] = *reinterpret_cast<const float4*>(
-            P.w_src + (int64_t)(task / kChunksPerSlice) * P.w_stride +
-            (int64_t)(s_first + j) * kSlice + (task % kChunksPerSlice) * kChunk + 4 * sub);
-    }
-    if constexpr (!kTf32) {
-      if (zero) {
-        constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
-        for (int idx = tid; idx < kWBufs * kUnits; idx += nthreads) {
-          const int w = idx / kUnits, u = idx % kUnits;
-          sts128(w_base + (uint32_t)w * MD::kBBytes + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
+    for (int q0 = 0; q0 < kMaxRounds; q0 += kBatch) {
+      if (q0 * groups >= kTasks) break;
+      float4 wv[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int task = (q0 + q) * groups + (tid >> 4);
+        wv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (task < kTasks)
+          wv[q] = *reinterpret_cast<const float4*>(
+              P.w_src + (int64_t)(task / kChunksPerSlice) * P.w_stride +
+              (int64_t)(s_first + j) * kSlice + (task % kChunksPerSlice) * kChunk + 4 * sub);
+      }
+      if constexpr (!kTf32) {
+        if (zero && q0 == 0) {
+          constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
+          for (int idx = tid; idx < kWBufs * kUnits; idx += nthreads) {
+            const int w = idx / kUnits, u = idx % kUnits;
+            sts128(w_base + (uint32_t)w * MD::kBBytes + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
+          }
         }
       }
-    }
 #pragma unroll
-    for (int q = 0; q < kMaxRounds; ++q) {  // uniform trip count: the shuffles need whole warps
-      const int task = q * groups + (tid >> 4);
-      if (q * groups >= kTasks) break;
-      const bool active = task < kTasks;
-      const int t = active ? task : 0;
-      convert_w4<kTf32>(wv[q], t / kChunksPerSlice, sub, wbuf(j % kSlots, t % kChunksPerSlice),
-                        active);
+      for (int q = 0; q < kBatch; ++q) {  // uniform trip count: the shuffles need whole warps
+        const int task = (q0 + q) * groups + (tid >> 4);
+        if ((q0 + q) * groups >= kTasks) break;
+        const bool active = task < kTasks;
+        const int t = active ? task : 0;
+        convert_w4<kTf32>(wv[q], t / kChunksPerSlice, sub, wbuf(j % kSlots, t % kChunksPerSlice),
+                          active);
+      }
     }
   };
 
-  // ---- set-up.  Thread 0 initialises the barriers and starts the first x
-  // loads (and, with prepacked limbs, the W loads of the first two slices);
-  // warp 1 allocates TMEM; warps 2..15 zero the W buffers' zero rows and
-  // convert the first slice's fp32 W, while the first x loads are in flight.
-  if (threadIdx.x == 0) {
-    // the x barriers first, so that the first x loads leave at once
-    for (int s = 0; s < kXStages; ++s) {
-      mbar_init(smem_u32(&bk.full_x[s]), 1);
-      mbar_init(smem_u32(&bk.empty_x[s]), kNumTWarps);
-    }
-    fence_mbarrier_init();
-    {
-      const uint64_t pol = l2_policy_evict_first();
-      for (int L = 0; L < kXStages && L < n_loads; ++L) issue_x_load(L, pol);
-    }
-    // mma_ready[k % 4]: the four transform warps of chunk k and the four
-    // accumulate warps once they have read chunk k - 4 (for the first four
-    // chunks, those four arrivals are made here)
-    for (int d = 0; d < kNumD; ++d) {
-      mbar_init(smem_u32(&bk.mma_ready[d]), 8);
-      for (int q = 0; q < 4; ++q) mbar_arrive(smem_u32(&bk.mma_ready[d]));
-    }
-    for (int a = 0; a < kNumA; ++a) mbar_init(smem_u32(&bk.a_empty[a]), 1);  // MMA commit
-    for (int d = 0; d < kNumD; ++d) mbar_init(smem_u32(&bk.d_full[d]), 1);  // MMA commit
-    for (int q = 0; q < kNumSq; ++q) {
-      mbar_init(smem_u32(&bk.sq_full[q]), 4);     // the four transform warps of the chunk
-      mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the four accumulate warps
-    }
-    for (int w = 0; w < kWBufs; ++w) mbar_init(smem_u32(&bk.w_full[w]), 1);
-    for (int g = 0; g < kNumMma; ++g) mbar_init(smem_u32(&bk.drain[g]), 1);
-    bk.abort = 0;
-    bk.never = 0;
-    fence_mbarrier_init();
-    if constexpr (!kTf32) {
-      if (P.w_src == nullptr) {
-        prefetch_tensormap(&tmap_w);
-        const uint64_t wpol = l2_policy_evict_last();
-        for (int j = 0; j < kSlots && j < n_sl; ++j)
-          for (int c = 0; c < kChunksPerSlice; ++c) issue_w_load(j, c, s_first + j, wpol);
+  // ---- set-up.  Lane 0 of the x producer initialises the barriers (the x
+  // ones first) and starts the first x loads (and, with prepacked limbs, the
+  // W loads of the first two slices); warp 1 allocates TMEM; the transform
+  // and accumulate warps zero the W buffers' zero rows and convert the first
+  // slice's fp32 W while the first x loads are in flight.
+  if (warp == kXWarp) {
+    if (lane == 0) {
+      for (int s = 0; s < kXStages; ++s) {
+        mbar_init(smem_u32(&bk.full_x[s]), 1);
+        mbar_init(smem_u32(&bk.empty_x[s]), kNumTWarps);
+      }
+      fence_mbarrier_init();
+      {
+        const uint64_t pol = l2_policy_evict_first();
+        for (int L = 0; L < kXStages && L < n_loads; ++L) issue_x_load(L, pol);
+      }
+      // mma_ready[k % 3]: the four transform warps of chunk k and the eight
+      // accumulate warps once they have read chunk k - 3 (for the first three
+      // chunks, those eight arrivals are made here)
+      for (int c = 0; c < kNumMma; ++c) {
+        mbar_init(smem_u32(&bk.mma_ready[c]), 4 + kNumDWarps);
+        for (int q = 0; q < kNumDWarps; ++q) mbar_arrive(smem_u32(&bk.mma_ready[c]));
+      }
+      for (int a = 0; a < 2 * kNumA; ++a) mbar_init(smem_u32(&bk.a_empty[a]), 1);  // MMA commit
+      for (int d = 0; d < kNumD; ++d) mbar_init(smem_u32(&bk.d_full[d]), 1);  // MMA commit
+      for (int q = 0; q < kNumSq; ++q) {
+        mbar_init(smem_u32(&bk.sq_full[q]), 4);     // the four transform warps of the chunk
+        mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the accumulate warps that read the sums
+      }
+      for (int w = 0; w < kWBufs; ++w) mbar_init(smem_u32(&bk.w_full[w]), 1);
+      for (int g = 0; g < kNumMma; ++g) mbar_init(smem_u32(&bk.drain[g]), 1);
+      bk.abort = 0;
+      bk.never = 0;
+      fence_mbarrier_init();
+      if constexpr (!kTf32) {
+        if (P.w_src == nullptr) {
+          prefetch_tensormap(&tmap_w);
+          const uint64_t wpol = l2_policy_evict_last();
+          for (int j = 0; j < kSlots && j < n_sl; ++j)
+            for (int c = 0; c < kChunksPerSlice; ++c) issue_w_load(j, c, s_first + j, wpol);
+        }
       }
     }
-  } else if (warp == kMmaWarp0) {
+  } else if (warp == kTmemWarp) {
     tmem_alloc(smem_u32(&bk.tmem_base), kTmemCols);
     tmem_relinquish();
-  } else if (warp >= 2) {
-    const int tid = threadIdx.x - 64, nthr = kThreads - 64;
+  } else if (warp >= kFirstWorkWarp) {
+    const int tid = threadIdx.x - kFirstWorkWarp * 32, nthr = kThreads - kFirstWorkWarp * 32;
     if (P.w_src != nullptr) {
       convert_slice(0, tid, nthr, true);
     } else if constexpr (!kTf32) {  // prepacked limbs: only the zero rows
@@ -736,21 +764,57 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   tc_fence_before();
   cta_barrier();
   tc_fence_after();
-  if (threadIdx.x == 0 && P.w_src != nullptr)  // the first slice is in place
+  if (threadIdx.x == kFirstWorkWarp * 32 && P.w_src != nullptr)  // the first slice is in place
     for (int c = 0; c < kChunksPerSlice; ++c) mbar_arrive(smem_u32(&bk.w_full[c]));
   const uint32_t tmem = bk.tmem_base;
   const volatile int* abort_flag = &bk.abort;
   const volatile int* never = &bk.never;
 
-  if (warp == kXWarp) {
+  if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kNumMma) {
+    // ---------------- MMA issuers: warp t issues the chunks k with k % 3 ==
+    // t, into A and D buffer t.  Chunk k needs its A buffer written and its D
+    // buffer read (both on mma_ready[t], one poll) and its W buffer filled
+    // (w_full: once filled it stays so until every MMA of the slice is done,
+    // so the wait returns at once after the first).  mma_ready[t] is this
+    // warp's own barrier, so it has seen every earlier phase, as a parity
+    // wait needs; a W barrier's earlier fill has always completed before any
+    // issuer waits for its next one.  Each chunk commits twice: D complete
+    // (d_full) and A free again (a_empty).  The whole warp runs the loop, the
+    // waits are warp votes and one elected lane issues each MMA and commit.
+    const int t = warp - kMmaWarp0;
+    bool ok = true;
+    for (int k = t; ok && k < n_chunks; k += kNumMma) {
+      const int i = k / kChunksPerSlice, c = k % kChunksPerSlice;
+      const int j = unit_slice(i) - s_first, slot = j % kSlots;
+      bool got = mbar_wait(smem_u32(&bk.mma_ready[t]), (uint32_t)(k / kNumMma) & 1u, abort_flag,
+                           kWaitLimitNs);
+      got = got && mbar_wait(smem_u32(&bk.w_full[slot * kChunksPerSlice + c]),
+                             (uint32_t)(j / kSlots) & 1u, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, got);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a = tmem + (uint32_t)t * kACols;
+      const uint32_t d = tmem + kDCol0 + (uint32_t)t * kDCols<kTf32>;
+      const uint64_t bdesc = smem_desc_sw128(wbuf(slot, c));
+      if constexpr (kTf32)
+        mma_chunk_tf32x3(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t]));
+      else
+        mma_chunk_exact(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t]));
+      umma_commit_warp(smem_u32(&bk.a_empty[t * 2 + (k & 1)]));
+    }
+    if (!ok && lane == 0) fail(bk, P.err);
+    // every MMA this warp issued completes before TMEM is released
+    umma_commit_warp(smem_u32(&bk.drain[t]));
+    mbar_wait(smem_u32(&bk.drain[t]), 0, never, kDrainLimitNs);
+  } else if (warp == kXWarp) {
     // ---------------- x producer: the loads after the first kXStages, each
-    // once the transform warps of its stage have read it
+    // once the transform warps have read the stage's previous load
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       int L = kXStages;
       for (; L < n_loads; ++L) {
         const int st = L % kXStages;
-        if (!mbar_wait(smem_u32(&bk.empty_x[st]), ((uint32_t)(L / kXStages) & 1u) ^ 1u, abort_flag,
+        if (!mbar_wait(smem_u32(&bk.empty_x[st]), (uint32_t)(L / kXStages - 1) & 1u, abort_flag,
                        kWaitLimitNs)) {
           fail(bk, P.err);
           break;
@@ -762,55 +826,14 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         mbar_wait(smem_u32(&bk.full_x[j % kXStages]), (uint32_t)(j / kXStages) & 1u, never,
                   kDrainLimitNs);
     }
-  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kNumMma) {
-    // ---------------- MMA issuers: warp 1 + c issues chunk c of every unit,
-    // into D buffer c with W buffer (slot, c).  An issuing thread's
-    // shared-memory accesses, its mbarrier waits included, wait behind the
-    // MMAs it has queued, so one issuer cannot queue its next chunk before its
-    // previous one completes; four take turns and keep the tensor pipe busy.
-    // Chunk k needs its A buffer written and its D buffer read (both on
-    // mma_ready, one poll) and, in the first unit of a slice, its W buffer
-    // filled (w_full).  Each barrier it waits on is its own, so it has seen
-    // every earlier phase, as a parity wait needs.  Each chunk commits twice:
-    // D complete (d_full) and A free again (a_empty).  The whole warp runs
-    // the loop, the waits are warp votes and one elected lane issues each MMA
-    // and commit.
-    const int c = warp - kMmaWarp0;
-    bool ok = true;
-    int prev_slice = -1;
-    for (int i = 0; ok && i < n; ++i) {
-      const int k = kChunksPerSlice * i + c;
-      const int s = unit_slice(i), j = s - s_first, slot = j % kSlots;
-      const bool first_use = s != prev_slice;
-      prev_slice = s;
-      bool got = mbar_wait(smem_u32(&bk.mma_ready[c]), (uint32_t)i & 1u, abort_flag, kWaitLimitNs);
-      if (first_use)
-        got = got && mbar_wait(smem_u32(&bk.w_full[slot * kChunksPerSlice + c]),
-                               (uint32_t)(j / kSlots) & 1u, abort_flag, kWaitLimitNs);
-      ok = __all_sync(0xffffffffu, got);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t a = tmem + (uint32_t)(k % kNumA) * kACols;
-      const uint32_t d = tmem + kDCol0 + (uint32_t)c * kDCols<kTf32>;
-      const uint64_t bdesc = smem_desc_sw128(wbuf(slot, c));
-      if constexpr (kTf32)
-        mma_chunk_tf32x3(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[c]));
-      else
-        mma_chunk_exact(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[c]));
-      umma_commit_warp(smem_u32(&bk.a_empty[k % kNumA]));
-    }
-    if (!ok && lane == 0) fail(bk, P.err);
-    // every MMA this warp issued completes before TMEM is released
-    umma_commit_warp(smem_u32(&bk.drain[c]));
-    mbar_wait(smem_u32(&bk.drain[c]), 0, never, kDrainLimitNs);
-  } else if (warp >= kFirstTWarp && warp < kFirstDWarp) {
+  } else if (warp >= kFirstTWarp && warp < kFirstTWarp + kNumTWarps) {
     // ---------------- transform warps: chunk k = 2L + h of x load L, into A
-    // buffer h.  A parity wait for phase p of an mbarrier is only sound when
-    // the waiter already knows phase p - 1 complete: earlier, the wait cannot
-    // tell p - 2 (same parity) from p and returns at once.  Every wait below
-    // follows that rule: on full_x / chunk_done / a_empty this half waited
-    // for the previous phase itself (a_empty[h] carries only this half's
-    // chunks).
+    // buffer k % 3.  A parity wait for phase p of an mbarrier is only sound
+    // when the waiter already knows phase p - 1 complete: earlier, the wait
+    // cannot tell p - 2 (same parity) from p and returns at once.  Every wait
+    // below follows that rule: on full_x / chunk_done this half waited for
+    // the previous phase itself, and a_empty[k % 3][1 - h] carries exactly the
+    // chunks k - 3 of this half's chunks k.
     const int h = (warp - kFirstTWarp) >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
@@ -871,9 +894,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       sq_buf[(k % kNumSq) * kTileM + row] = tsq;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bk.sq_full[k % kNumSq]));
-      if (k >= kNumA) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.a_empty[h]),
-                                               (uint32_t)(k / kNumA - 1) & 1u, abort_flag,
+      if (k >= kNumA) {  // chunk k - 3 (the other half's) is done with A buffer k % 3
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.a_empty[(k % kNumA) * 2 + (h ^ 1)]),
+                                               (uint32_t)((k - kNumA) / (2 * kNumA)) & 1u, abort_flag,
                                                kWaitLimitNs));
         if (!ok) break;
       }
@@ -884,18 +907,24 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bk.mma_ready[k % kNumD]));
+      if (lane == 0) mbar_arrive(smem_u32(&bk.mma_ready[k % kNumMma]));
     }
     if (!ok) fail(bk, P.err);
-  } else if (warp >= kFirstDWarp) {
-    // ---------------- accumulate warps: first the second slice's W (when the
-    // CTA has one), which is not needed before the first unit is done; then
-    // chunk dots into slice totals
+  } else if (warp >= kFirstDWarp && warp < kFirstDWarp + kNumDWarps) {
+    // ---------------- accumulate warps: warp 12 + 4 e + q reads, for the
+    // rows of quadrant q, the outputs 12 e .. 12 e + 11 of every chunk (its
+    // 4 x 12 D columns in one TMEM round trip), forms their chunk dots and
+    // adds them into the slice totals, chunks in order; group e = 0 also
+    // adds the sums of squares.  First all eight convert the second slice's
+    // W (when the CTA has one), which is not needed before the first unit is
+    // done.
+    const int e = (warp - kFirstDWarp) >> 2;
+    const int dtid = threadIdx.x - kFirstDWarp * 32;  // 0..255
     if (P.w_src != nullptr && n_sl >= 2) {
-      convert_slice(1, threadIdx.x - kFirstDWarp * 32, 4 * 32, false);
+      convert_slice(1, dtid, kNumDWarps * 32, false);
       fence_proxy_async_smem();
-      named_bar_sync(1, 4 * 32);
-      if (threadIdx.x == kFirstDWarp * 32)
+      named_bar_sync(1, kNumDWarps * 32);
+      if (dtid == 0)
         for (int c = 0; c < kChunksPerSlice; ++c)
           mbar_arrive(smem_u32(&bk.w_full[kChunksPerSlice + c]));
     }
@@ -905,14 +934,14 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     auto refill = [&](int jn) {
       const int slot = jn % kSlots;
       if (P.w_src != nullptr) {
-        convert_slice(jn, threadIdx.x - kFirstDWarp * 32, 4 * 32, false);
+        convert_slice(jn, dtid, kNumDWarps * 32, false);
         fence_proxy_async_smem();
-        named_bar_sync(1, 4 * 32);
-        if (threadIdx.x == kFirstDWarp * 32)
+        named_bar_sync(2, kNumDWarps * 32);
+        if (dtid == 0)
           for (int c = 0; c < kChunksPerSlice; ++c)
             mbar_arrive(smem_u32(&bk.w_full[slot * kChunksPerSlice + c]));
       } else if constexpr (!kTf32) {
-        if (threadIdx.x == kFirstDWarp * 32)
+        if (dtid == 0)
           for (int c = 0; c < kChunksPerSlice; ++c)
             issue_w_load(slot, c, s_first + jn, l2_policy_evict_last());
       }
@@ -921,48 +950,61 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const uint64_t keep = l2_policy_evict_last();  // the tail reads the partials next
-    float2 acc[kMix / 2];
-#pragma unroll
-    for (int j = 0; j < kMix / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-    float sqs = 0.0f;
+    constexpr int kOut = kMix / 2;  // outputs per group
     bool ok = true;
-    for (int k = 0; k < n_chunks; ++k) {
-      // D of chunk k complete, and the chunk's sum of squares in its slot
-      bool got = mbar_wait(smem_u32(&bk.d_full[k % kNumD]), (uint32_t)(k / kNumD) & 1u, abort_flag,
-                           kWaitLimitNs);
-      got = got && mbar_wait(smem_u32(&bk.sq_full[k % kNumSq]), (uint32_t)(k / kNumSq) & 1u,
+    for (int i = 0; ok && i < n; ++i) {
+      float2 acc[kOut / 2];
+#pragma unroll
+      for (int j = 0; j < kOut / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+      float sqs = 0.0f;
+      for (int c = 0; c < kChunksPerSlice; ++c) {
+        const int k = kChunksPerSlice * i + c;
+        // D of chunk k complete (and, for group 0, the chunk's sum of
+        // squares in its slot)
+        bool got = mbar_wait(smem_u32(&bk.d_full[k % kNumD]), (uint32_t)(k / kNumD) & 1u,
                              abort_flag, kWaitLimitNs);
-      ok = __all_sync(0xffffffffu, got);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_col = tmem + kDCol0 + (uint32_t)(k % kNumD) * kDCols<kTf32>;
-      const float tsq = sq_buf[(k % kNumSq) * kTileM + row];
-      if constexpr (kTf32) {
-        uint32_t dv[kMix];
-        tmem_ld16(lanes | d_col, dv);
-        tmem_ld8(lanes | (d_col + 16), dv + 16);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
-          mbar_arrive(smem_u32(&bk.mma_ready[k % kNumD]));  // D buffer free for chunk k + 4
-        }
-#pragma unroll
-        for (int j = 0; j < kMix / 2; ++j)
-          acc[j] = __fadd2_rn(acc[j], make_float2(__uint_as_float(dv[2 * j]),
-                                                  __uint_as_float(dv[2 * j + 1])));
-      } else {
-        // D = [top | r1 | r2 | r3] (24 columns each); chunk dot = top + ((r1 +
-        // r2) + r3).  Outputs 0..15 first, then 16..23 (two TMEM round trips
-        // keep the registers within the 512-thread budget).
-        {
-          uint32_t dv[4][16];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) tmem_ld16(lanes | (d_col + 24 * g), dv[g]);
+        if (e == 0)
+          got = got && mbar_wait(smem_u32(&bk.sq_full[k % kNumSq]), (uint32_t)(k / kNumSq) & 1u,
+                                 abort_flag, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, got);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_col = tmem + kDCol0 + (uint32_t)(k % kNumD) * kDCols<kTf32>;
+        const float tsq = e == 0 ? sq_buf[(k % kNumSq) * kTileM + row] : 0.0f;
+        if constexpr (kTf32) {
+          // D's first 24 columns are the chunk dots
+          uint32_t dv[kOut];
+          tmem_ld8(lanes | (d_col + kOut * e), dv);
+          tmem_ld4(lanes | (d_col + kOut * e + 8), dv + 8);
           tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (e == 0) mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
+            mbar_arrive(smem_u32(&bk.mma_ready[k % kNumMma]));  // D buffer free for chunk k + 3
+          }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < kOut / 2; ++j)
+            acc[j] = __fadd2_rn(acc[j], make_float2(__uint_as_float(dv[2 * j]),
+                                                    __uint_as_float(dv[2 * j + 1])));
+        } else {
+          // D = [top | r1 | r2 | r3] (24 columns each); chunk dot = top + ((r1
+          // + r2) + r3), for this group's 12 outputs of each
+          uint32_t dv[4][kOut];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            tmem_ld8(lanes | (d_col + kMix * g + kOut * e), dv[g]);
+            tmem_ld4(lanes | (d_col + kMix * g + kOut * e + 8), dv[g] + 8);
+          }
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (e == 0) mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
+            mbar_arrive(smem_u32(&bk.mma_ready[k % kNumMma]));  // D buffer free for chunk k + 3
+          }
+#pragma unroll
+          for (int j = 0; j < kOut / 2; ++j) {
             const float2 top = make_float2(__uint_as_float(dv[0][2 * j]), __uint_as_float(dv[0][2 * j + 1]));
             const float2 u = make_float2(__uint_as_float(dv[1][2 * j]), __uint_as_float(dv[1][2 * j + 1]));
             const float2 v = make_float2(__uint_as_float(dv[2][2 * j]), __uint_as_float(dv[2][2 * j + 1]));
@@ -970,49 +1012,25 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
             acc[j] = __fadd2_rn(acc[j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
           }
         }
-        {
-          uint32_t dv[4][8];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) tmem_ld8(lanes | (d_col + 24 * g + 16), dv[g]);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
-            mbar_arrive(smem_u32(&bk.mma_ready[k % kNumD]));  // D buffer free for chunk k + 4
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 top = make_float2(__uint_as_float(dv[0][2 * j]), __uint_as_float(dv[0][2 * j + 1]));
-            const float2 u = make_float2(__uint_as_float(dv[1][2 * j]), __uint_as_float(dv[1][2 * j + 1]));
-            const float2 v = make_float2(__uint_as_float(dv[2][2 * j]), __uint_as_float(dv[2][2 * j + 1]));
-            const float2 w = make_float2(__uint_as_float(dv[3][2 * j]), __uint_as_float(dv[3][2 * j + 1]));
-            acc[8 + j] = __fadd2_rn(acc[8 + j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
-          }
-        }
+        sqs = __fadd_rn(sqs, tsq);
       }
-      sqs = __fadd_rn(sqs, tsq);
-      if (k % kChunksPerSlice == kChunksPerSlice - 1) {
-        const int i = k / kChunksPerSlice;
-        float* p = P.part + part_index(unit_tile(i) * kTileM + row, unit_slice(i), 0, P.n_slices);
+      if (!ok) break;
+      float* p = P.part + part_index(unit_tile(i) * kTileM + row, unit_slice(i), 0, P.n_slices);
 #pragma unroll
-        for (int j = 0; j < kMix / 2; ++j) {
-          stg_f32_hint(p + 8 * (2 * j), acc[j].x, keep);
-          stg_f32_hint(p + 8 * (2 * j + 1), acc[j].y, keep);
-          acc[j] = make_float2(0.0f, 0.0f);
-        }
-        stg_f32_hint(p + 8 * kMix, sqs, keep);
-        sqs = 0.0f;
-        // the last unit of slice j done: slice j + 2 (if any) may take its slot
-        const int j = unit_slice(i) - s_first;
-        if (j + kSlots < n_sl && (i == n - 1 || unit_slice(i + 1) != unit_slice(i)))
-          refill(j + kSlots);
+      for (int j = 0; j < kOut / 2; ++j) {
+        stg_f32_hint(p + 8 * (kOut * e + 2 * j), acc[j].x, keep);
+        stg_f32_hint(p + 8 * (kOut * e + 2 * j + 1), acc[j].y, keep);
       }
+      if (e == 0) stg_f32_hint(p + 8 * kMix, sqs, keep);
+      // the last unit of slice j done: slice j + 2 (if any) may take its slot
+      const int j = unit_slice(i) - s_first;
+      if (j + kSlots < n_sl && (i == n - 1 || unit_slice(i + 1) != unit_slice(i)))
+        refill(j + kSlots);
     }
     if (!ok) fail(bk, P.err);
     if constexpr (!kTf32) {
       // the TMA loads of prepacked limbs complete before the CTA can exit
-      if (P.w_src == nullptr && threadIdx.x == kFirstDWarp * 32)
+      if (P.w_src == nullptr && dtid == 0)
         for (int j = max(0, n_sl - kSlots); j < n_sl; ++j)
           for (int c = 0; c < kChunksPerSlice; ++c)
             mbar_wait(smem_u32(&bk.w_full[(j % kSlots) * kChunksPerSlice + c]),
@@ -1023,7 +1041,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   // ---- every role has finished (or given up); TMEM is no longer needed
   tc_fence_before();
   cta_barrier();
-  if (warp == kMmaWarp0) {
+  if (warp == kTmemWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -1,25 +1,29 @@
 """The tensor-core kernel's hand-off protocol, checked on the CPU.
 
-The kernel's roles (x producer, two halves of four transform warps, four MMA
-issuers, four accumulate warps, the W-slot refills) hand chunks to each other
-through mbarriers whose waits only test the parity of the phase they want.
-Such a wait is sound only when the waiter already knows the phase before it
-complete; otherwise it cannot tell phase p - 2 from phase p and returns early.
-This module restates, role by role, the waits and arrivals of
-hyper_connection_mix_gb300/csrc/hcmix_tc.cuh as a model with real parity
-semantics (the barrier's phase counter, arrival counts, a wait that returns
-when the current phase parity differs), runs it under random interleavings
-with the MMAs completing in issue order and the x loads landing in any order,
-and asserts for every wait that the exact phase it needed had completed, and
-that every run finishes.  It is a model of the kernel's protocol, kept beside
-the kernel; the GPU tests check the kernel itself.
+The kernel's roles (the x producer, two halves of four transform warps, three
+MMA issuers, two output groups of four accumulate warps, the W-slot refills) hand chunks to each other through mbarriers whose waits only test the
+parity of the phase they want.  Such a wait is sound only when the waiter
+already knows the phase before it complete; otherwise it cannot tell phase
+p - 2 from phase p and returns early.  This module restates, role by role, the
+waits and arrivals of hyper_connection_mix_gb300/csrc/hcmix_tc.cuh as a model
+with real parity semantics (the barrier's phase counter, arrival counts, a
+wait that returns when the current phase parity differs), runs it under random
+interleavings with the MMAs completing in issue order and the x loads landing
+in any order, and asserts
+  * for every wait, that the exact phase it needed had completed;
+  * for every buffer (x stage, TMEM A and D buffers, sum-of-squares slot, W
+    slot), that it is only rewritten once every reader of its previous
+    contents is done;
+  * that every run finishes.
+It is a model of the kernel's protocol, kept beside the kernel; the GPU tests
+check the kernel itself.
 """
 import random
 
 import pytest
 
-X_STAGES, N_A, N_D, N_SQ, SLOTS, N_MMA = 3, 2, 4, 8, 2, 4
-SHARED_A_EMPTY = False  # a planted mistake for the test that checks the model has teeth
+X_STAGES, N_A, N_D, N_SQ, SLOTS, N_MMA = 3, 3, 3, 8, 2, 3
+PLANTED = None  # a planted mistake for the tests that check the model has teeth
 
 
 class Bar:
@@ -36,7 +40,7 @@ class Bar:
 
 def run_cta(u_begin, n, n_tiles, seed, packed=False):
     """One CTA's units [u_begin, u_begin + n) of a grid with n_tiles tiles per
-    slice.  Returns the list of aliasing errors (empty when sound); raises on a
+    slice.  Returns the list of errors (empty when sound); raises on a
     deadlock."""
     rnd = random.Random(seed)
     sl = [(u_begin + i) // n_tiles for i in range(n)]
@@ -45,16 +49,24 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     nck, nld = 4 * n, 2 * n
     mk = lambda p, c, m: [Bar(c, f"{p}{i}") for i in range(m)]
     full_x, empty_x = mk("full_x", 1, X_STAGES), mk("empty_x", 8, X_STAGES)
-    # mma_ready[k % 4]: the transform warps of chunk k (4) and the accumulate
-    # warps once they have read chunk k - 4 (4; made at set-up for k < 4)
-    mma_ready, a_empty = mk("mma_ready", 8, N_D), mk("a_empty", 1, N_A)
+    # mma_ready[k % 3]: the four transform warps of chunk k and the eight
+    # accumulate warps once they have read chunk k - 3 (made at set-up for k < 3)
+    mma_ready = mk("mma_ready", 12, N_MMA)
     for b in mma_ready:
-        for _ in range(4):
+        for _ in range(8):
             b.arrive()
+    a_empty = mk("a_empty", 1, 2 * N_A)  # [k % 3 * 2 + k % 2]: chunk k's MMAs done
     sq_full, chunk_done = mk("sq_full", 4, N_SQ), mk("chunk_done", 4, N_SQ)
     d_full, w_full = mk("d_full", 1, N_D), mk("w_full", 1, 4 * SLOTS)
-    dconv = Bar(4, "dconv")
+    dconv = Bar(8, "dconv")
     errors, pipe, tma = [], [], []
+    # progress, for the buffer checks
+    x_read = [0] * nld          # transform warps that have read x load L
+    mma_done = set()            # chunks whose MMAs completed
+    d_read = [0] * nck          # accumulate warps that have read D of chunk k
+    sq_read = [0] * nck         # accumulate warps that have read the sum of squares of chunk k
+    refill_bar = Bar(8, "refill")
+    slice_done = set()          # slices whose every MMA completed (W slot free)
 
     def wait(bar, phase, who):
         parity = phase & 1
@@ -63,12 +75,18 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
         if bar.phase <= phase:
             errors.append(f"{who}: {bar.name} wanted phase {phase}, barrier at {bar.phase}")
 
+    def check(cond, what):
+        if not cond:
+            errors.append(what)
+
+    def issue_load(L):
+        check(L < X_STAGES or x_read[L - X_STAGES] == 8, f"x load {L} over an unread stage")
+        tma.append((L % X_STAGES, L))
+
     def x_producer():
-        for L in range(nld):
-            st = L % X_STAGES
-            if L >= X_STAGES:
-                yield from wait(empty_x[st], L // X_STAGES - 1, f"x L{L}")
-            tma.append(st)
+        for L in range(X_STAGES, nld):
+            yield from wait(empty_x[L % X_STAGES], L // X_STAGES - 1, f"x L{L}")
+            issue_load(L)
             yield None
 
     def transform(h, q):
@@ -76,60 +94,76 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
             k, st = 2 * L + h, L % X_STAGES
             yield from wait(full_x[st], L // X_STAGES, f"T{h}{q} k{k} x")
             yield None
+            x_read[L] += 1
             empty_x[st].arrive()
             if k >= N_SQ:
                 yield from wait(chunk_done[k % N_SQ], k // N_SQ - 1, f"T{h}{q} k{k} sq")
+                check(sq_read[k - N_SQ] == 4, f"sq slot of chunk {k} over an unread one")
             sq_full[k % N_SQ].arrive()
-            if k >= N_A:  # A buffer h, last used by chunk k - 2
-                if SHARED_A_EMPTY:  # planted: one barrier for both halves' chunks
-                    yield from wait(a_empty[0], k - 2, f"T{h}{q} k{k} A")
-                else:
-                    yield from wait(a_empty[h], k // N_A - 1, f"T{h}{q} k{k} A")
+            if k >= N_A:  # chunk k - 3 (the other half's) is done with A buffer k % 3
+                e = h if PLANTED == "own_half_a_empty" else h ^ 1
+                yield from wait(a_empty[(k % N_A) * 2 + e], (k - N_A) // (2 * N_A), f"T{h}{q} k{k} A")
+                check(k - N_A in mma_done, f"A buffer of chunk {k} rewritten before the MMAs of {k - N_A} were done")
             yield None
-            mma_ready[k % N_D].arrive()
+            mma_ready[k % N_MMA].arrive()
 
-    def issuer(c):  # chunk c of every unit
-        prev = -1
-        for i in range(n):
-            k = 4 * i + c
+    def issuer(t):  # the chunks k with k % 3 == t
+        for k in range(t, nck, N_MMA):
+            i, c = divmod(k, 4)
             s = sl[i]
             j = s - s_first
-            first = s != prev
-            prev = s
-            yield from wait(mma_ready[c], i, f"I{c} k{k} ready")
-            if first:
-                yield from wait(w_full[(j % SLOTS) * 4 + c], j // SLOTS, f"I{c} k{k} W")
+            yield from wait(mma_ready[t], k // N_MMA, f"I{t} k{k} ready")
+            # a W barrier: its earlier fill always completed before any issuer
+            # waits for the next, so several issuers may wait on it
+            yield from wait(w_full[(j % SLOTS) * 4 + c], j // SLOTS, f"I{t} k{k} W")
+            check(k < N_D or d_read[k - N_D] == 8, f"D buffer of chunk {k} over an unread one")
+            check(j < SLOTS or (s - SLOTS) in slice_done, f"chunk {k} reads a W slot being refilled")
             yield None
             pipe.append(k)
 
-    def accumulate(q):
-        if not packed and n_sl >= 2:  # the second slice, converted during set-up
+    def accumulate(e, q):  # outputs 12 e.. of quadrant q
+        if not packed and n_sl >= 2:  # the second slice, converted during set-up by all eight
             yield None
             dconv.arrive()
             while dconv.phase == 0:
                 yield (dconv, 0)
-            if q == 0:
+            if e == 0 and q == 0:
                 for c in range(4):
                     w_full[4 + c].arrive()
-        for k in range(nck):
-            yield from wait(d_full[k % N_D], k // N_D, f"D{q} k{k}")
-            yield from wait(sq_full[k % N_SQ], k // N_SQ, f"D{q} k{k} sq")
-            yield None
-            chunk_done[k % N_SQ].arrive()
-            mma_ready[k % N_D].arrive()  # D buffer k % 4 free for chunk k + 4
-            i = k // 4
-            if k % 4 == 3:
-                j = sl[i] - s_first
-                if j + SLOTS < n_sl and (i == n - 1 or sl[i + 1] != sl[i]) and q == 0:
-                    for c in range(4):  # refill: slice j + 2 into slot j % 2
+        for i in range(n):
+            for c in range(4):
+                k = 4 * i + c
+                dbar = k % N_D if PLANTED != "d_full_by_issuer" else c % N_D
+                yield from wait(d_full[dbar], k // N_D, f"D{e}{q} k{k}")
+                if e == 0:
+                    yield from wait(sq_full[k % N_SQ], k // N_SQ, f"D{e}{q} k{k} sq")
+                check(k in mma_done, f"D of chunk {k} read before its MMAs completed")
+                yield None
+                d_read[k] += 1
+                if e == 0:
+                    sq_read[k] += 1
+                    chunk_done[k % N_SQ].arrive()
+                mma_ready[k % N_MMA].arrive()  # D buffer free for chunk k + 3
+            j = sl[i] - s_first
+            if j + SLOTS < n_sl and (i == n - 1 or sl[i + 1] != sl[i]):
+                # refill by all eight (a named barrier), then one arrival
+                target = refill_bar.phase + 1  # the phase this arrival belongs to completes
+                refill_bar.arrive()
+                while refill_bar.phase < target:
+                    yield (refill_bar, (target - 1) & 1)
+                if e == 0 and q == 0:
+                    slice_done.add(sl[i])
+                    for c in range(4):  # slice j + 2 into slot j % 2
                         w_full[((j + SLOTS) % SLOTS) * 4 + c].arrive()
 
     for c in range(4 * min(SLOTS, n_sl) if packed else 4):
         w_full[c].arrive()  # set-up: the first slice (and the second, prepacked)
+    for L in range(min(X_STAGES, nld)):  # set-up: the first x loads
+        issue_load(L)
     roles = {"x": x_producer()}
     roles.update({f"I{g}": issuer(g) for g in range(N_MMA)})
     roles.update({f"T{h}{q}": transform(h, q) for h in (0, 1) for q in range(4)})
-    roles.update({f"D{q}": accumulate(q) for q in range(4)})
+    roles.update({f"D{e}{q}": accumulate(e, q) for e in (0, 1) for q in range(4)})
     state = {r: None for r in roles}
     done = set()
     while True:
@@ -138,10 +172,12 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
         if (pipe or tma) and (not ready or rnd.random() < 0.3):
             if pipe and (not tma or rnd.random() < 0.5):
                 k = pipe.pop(0)  # the tensor pipe completes MMAs in issue order
+                mma_done.add(k)
                 d_full[k % N_D].arrive()
-                a_empty[0 if SHARED_A_EMPTY else k % N_A].arrive()
+                a_empty[(k % N_A) * 2 + k % 2].arrive()
             else:
-                full_x[tma.pop(rnd.randrange(len(tma)))].arrive()
+                st, _ = tma.pop(rnd.randrange(len(tma)))
+                full_x[st].arrive()
             continue
         if not ready:
             assert len(done) == len(roles), \
@@ -161,28 +197,34 @@ def grid_ctas(M, K, sms=152):
     return [(b * U // G, (b + 1) * U // G - b * U // G, n_tiles) for b in range(G)]
 
 
+def distinct_shapes(M, K):
+    shapes = {}
+    for ub, n, nt in grid_ctas(M, K):
+        key = (n, tuple((ub + i) // nt - ub // nt for i in range(n)))
+        shapes.setdefault(key, (ub, n, nt))
+    return list(shapes.values())
+
+
 @pytest.mark.parametrize("M,K", [(1, 20480), (4096, 20480), (512, 20480), (130, 131072),
                                  (5, 131072), (256, 65536)])
 def test_protocol_sound_and_deadlock_free(M, K):
-    ctas = grid_ctas(M, K)
     # every distinct CTA shape (units, slice boundaries relative to the range)
-    shapes = {}
-    for ub, n, nt in ctas:
-        key = (n, tuple((ub + i) // nt - ub // nt for i in range(n)))
-        shapes.setdefault(key, (ub, n, nt))
-    for ub, n, nt in shapes.values():
+    for ub, n, nt in distinct_shapes(M, K):
         for seed in range(6):
             for packed in (False, True):
                 errs = run_cta(ub, n, nt, seed, packed)
                 assert not errs, f"M={M} K={K} units {ub}+{n} seed {seed}: {errs[:3]}"
 
 
-def test_model_catches_an_unordered_parity_wait():
-    """The check has teeth: with one a_empty barrier shared by both halves of
-    the transform warps (each half then sees only every other phase) the model
-    reports an early return or the deadlock it leads to."""
-    global SHARED_A_EMPTY
-    SHARED_A_EMPTY = True
+@pytest.mark.parametrize("mistake", ["own_half_a_empty", "d_full_by_issuer"])
+def test_model_catches_planted_mistakes(mistake):
+    """The checks have teeth: a transform half that waits for its own previous
+    chunk on A buffer k % 3 (instead of chunk k - 3, the other half's), or
+    accumulate warps that wait on the D barrier of the issuer rather than of
+    the buffer, are reported (an early return, a buffer rewritten too soon, or
+    the deadlock they lead to)."""
+    global PLANTED
+    PLANTED = mistake
     found = False
     try:
         for ub, n, nt in grid_ctas(4096, 20480)[:8]:
@@ -192,5 +234,5 @@ def test_model_catches_an_unordered_parity_wait():
                 except AssertionError:
                     found = True
     finally:
-        SHARED_A_EMPTY = False
+        PLANTED = None
     assert found
