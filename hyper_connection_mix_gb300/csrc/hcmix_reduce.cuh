@@ -20,26 +20,89 @@ constexpr int kReduceRows = 32;
 constexpr int kReduceThreads = 32 * kPartStride;
 constexpr int kReduceBatch = 40;
 
-// 1 / s for a Sinkhorn normalisation, by which the row's (column's) four
-// entries are then multiplied: the approximate reciprocal (within 1 ulp over
-// the whole range, subnormal s included, since the non-.ftz form keeps
-// subnormals; with the product, each entry is within 2 ulp of c / s, and the
-// iteration's own contraction keeps the result within a few ulp of the
-// correctly rounded sequence).  No branch: a data-dependent branch around a
-// division here made each Sinkhorn round ~10x slower.
-__device__ __forceinline__ float sinkhorn_rcp(float s) {
+// Fast transcendentals of the epilogue.  Each is within a few ulp of the
+// exact value, far inside the 1e-5 absolute tolerance of pre / post / comb
+// (values of order 1); the GPU tests hold the results to that tolerance
+// against the oracle.
+//   * rcp_fast: the approximate reciprocal (max error 1 ulp; a subnormal
+//     input flushes to zero and gives an infinity, which the callers exclude
+//     or redo);
+//   * exp_fast(x) = 2^(x log2 e), the product x log2 e carried to double
+//     length (its rounding error e enters as the factor 1 + e ln 2), then the
+//     approximate 2^t (max relative error 2^-22.5);
+//   * rsqrt_fast: the approximate 1/sqrt (max relative error 2^-22.9).
+__device__ __forceinline__ float rcp_fast(float s) {
   float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
   return r;
+}
+__device__ __forceinline__ float exp_fast(float x) {
+  constexpr float kLog2e = 1.44269502f, kLog2eLo = 1.92596299e-08f;  // log2 e = kLog2e + kLog2eLo
+  constexpr float kLn2 = 0.693147182f;
+  const float t = __fmul_rn(x, kLog2e);
+  const float e = __fadd_rn(__fmaf_rn(x, kLog2e, -t), __fmul_rn(x, kLog2eLo));
+  float p;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(p) : "f"(t));  // (subnormal results kept)
+  return __fmul_rn(p, __fmaf_rn(e, kLn2, 1.0f));
+}
+__device__ __forceinline__ float rsqrt_fast(float v) {
+  float r;
+  asm("rsqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Sinkhorn rounds (row normalisation, then column normalisation, sums in
+// index order, the reciprocal of each sum multiplied in) on the comb matrix
+// held as row-major pairs P[i][h] = (c[i][2h], c[i][2h+1]), so that the
+// column sums and every scaling run on packed pairs.  With kEps, hc_eps is
+// added to every sum (every sum is of non-negative values, so without it the
+// sums are unchanged).  A sum below the normal range gives an infinite
+// reciprocal, which leaves an infinity or NaN in the matrix: the caller checks
+// for that and redoes the rounds with kDivide, which divides each entry by
+// its sum (IEEE, as the oracle does) instead.
+template <bool kDivide, bool kEps>
+__device__ __forceinline__ void sinkhorn_rounds(float2 (&P)[kHc][kHc / 2], int iters, float hc_eps) {
+  static_assert(kHc == 4, "four-by-four comb");
+  const float2 eps2 = make_float2(hc_eps, hc_eps);
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < kHc; ++i) {
+      float s = __fadd_rn(__fadd_rn(__fadd_rn(P[i][0].x, P[i][0].y), P[i][1].x), P[i][1].y);
+      if constexpr (kEps) s = __fadd_rn(s, hc_eps);
+      if constexpr (kDivide) {
+#pragma unroll
+        for (int h = 0; h < kHc / 2; ++h)
+          P[i][h] = make_float2(__fdiv_rn(P[i][h].x, s), __fdiv_rn(P[i][h].y, s));
+      } else {
+        const float rs = rcp_fast(s);
+        const float2 rs2 = make_float2(rs, rs);
+        P[i][0] = __fmul2_rn(P[i][0], rs2);
+        P[i][1] = __fmul2_rn(P[i][1], rs2);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kHc / 2; ++h) {
+      float2 s = __fadd2_rn(__fadd2_rn(__fadd2_rn(P[0][h], P[1][h]), P[2][h]), P[3][h]);
+      if constexpr (kEps) s = __fadd2_rn(s, eps2);
+      if constexpr (kDivide) {
+#pragma unroll
+        for (int i = 0; i < kHc; ++i)
+          P[i][h] = make_float2(__fdiv_rn(P[i][h].x, s.x), __fdiv_rn(P[i][h].y, s.y));
+      } else {
+        const float2 rs = make_float2(rcp_fast(s.x), rcp_fast(s.y));
+#pragma unroll
+        for (int i = 0; i < kHc; ++i) P[i][h] = __fmul2_rn(P[i][h], rs);
+      }
+    }
+  }
 }
 
 // The epilogue of one row, by one thread, from the row's totals (s_tot[j][r]:
 // j < 24 mix, j = 24 sum of squares): r = 1/sqrt(sq (1/K) + rms_eps); logit
 // j = mix_j r scale[g(j)] + base_j; pre = sigmoid, post = 2 sigmoid;
 // Sinkhorn on exp of the 16 comb logits, rows then columns, sums in index
-// order.  The row and column reciprocals of a normalisation are taken once
-// (sinkhorn_rcp) and multiplied in.  Rows at or past
-// row_end are not written.
+// order.  (hc_eps is added to every sum; the workloads use 0.)  Rows at or
+// past row_end are not written.
 __device__ __forceinline__ void epilogue_row(const float (&s_tot)[kPartStride][kReduceRows + 1],
                                              int r, int row, int row_end, float inv_k,
                                              const float* __restrict__ hc_scale,
@@ -48,41 +111,39 @@ __device__ __forceinline__ void epilogue_row(const float (&s_tot)[kPartStride][k
                                              float* __restrict__ pre, float* __restrict__ post,
                                              float* __restrict__ comb) {
   const float v = __fadd_rn(__fmul_rn(s_tot[kMix][r], inv_k), rms_eps);
-  const float rr = __fdiv_rn(1.0f, __fsqrt_rn(v));
+  const float rr = rsqrt_fast(v);
   float pp[2 * kHc];
 #pragma unroll
   for (int e = 0; e < 2 * kHc; ++e) {
     const float sc = e < kHc ? hc_scale[0] : hc_scale[1];
     const float lg = __fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][r], rr), sc), hc_base[e]);
-    pp[e] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lg)));
+    pp[e] = rcp_fast(__fadd_rn(1.0f, exp_fast(-lg)));  // (1 + e^-lg >= 1: no subnormal input)
   }
-  float c[kHc][kHc];
+  auto comb_init = [&](float2 (&P)[kHc][kHc / 2]) {
 #pragma unroll
-  for (int i = 0; i < kHc; ++i)
+    for (int i = 0; i < kHc; ++i)
 #pragma unroll
-    for (int jj = 0; jj < kHc; ++jj) {
-      const int e = 2 * kHc + kHc * i + jj;
-      c[i][jj] = expf(__fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][r], rr), hc_scale[2]), hc_base[e]));
-    }
-  // every sum is of positive values, so s + 0 = s: the eps add is skipped at 0
-  const bool add_eps = hc_eps != 0.0f;
-  for (int it = 0; it < iters; ++it) {
+      for (int h = 0; h < kHc / 2; ++h) {
+        const int e = 2 * kHc + kHc * i + 2 * h;
+        P[i][h] = make_float2(
+            exp_fast(__fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][r], rr), hc_scale[2]), hc_base[e])),
+            exp_fast(__fadd_rn(__fmul_rn(__fmul_rn(s_tot[e + 1][r], rr), hc_scale[2]), hc_base[e + 1])));
+      }
+  };
+  float2 P[kHc][kHc / 2];
+  comb_init(P);
+  if (hc_eps != 0.0f)
+    sinkhorn_rounds<false, true>(P, iters, hc_eps);
+  else
+    sinkhorn_rounds<false, false>(P, iters, hc_eps);
+  float check = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kHc; ++i) {
-      float s = __fadd_rn(__fadd_rn(__fadd_rn(c[i][0], c[i][1]), c[i][2]), c[i][3]);
-      if (add_eps) s = __fadd_rn(s, hc_eps);
-      const float rs = sinkhorn_rcp(s);
-#pragma unroll
-      for (int jj = 0; jj < kHc; ++jj) c[i][jj] = __fmul_rn(c[i][jj], rs);
-    }
-#pragma unroll
-    for (int jj = 0; jj < kHc; ++jj) {
-      float s = __fadd_rn(__fadd_rn(__fadd_rn(c[0][jj], c[1][jj]), c[2][jj]), c[3][jj]);
-      if (add_eps) s = __fadd_rn(s, hc_eps);
-      const float rs = sinkhorn_rcp(s);
-#pragma unroll
-      for (int i = 0; i < kHc; ++i) c[i][jj] = __fmul_rn(c[i][jj], rs);
-    }
+  for (int i = 0; i < kHc; ++i) check += (P[i][0].x + P[i][0].y) + (P[i][1].x + P[i][1].y);
+  if (!isfinite(check)) {
+    // a sum fell below the normal range (or the inputs hold an infinity or
+    // NaN): again, dividing by the sums
+    comb_init(P);
+    sinkhorn_rounds<true, true>(P, iters, hc_eps);
   }
   if (row >= row_end) return;
 #pragma unroll
@@ -93,7 +154,10 @@ __device__ __forceinline__ void epilogue_row(const float (&s_tot)[kPartStride][k
 #pragma unroll
   for (int i = 0; i < kHc; ++i)
 #pragma unroll
-    for (int jj = 0; jj < kHc; ++jj) comb[(int64_t)row * kHc * kHc + kHc * i + jj] = c[i][jj];
+    for (int h = 0; h < kHc / 2; ++h) {
+      comb[(int64_t)row * kHc * kHc + kHc * i + 2 * h] = P[i][h].x;
+      comb[(int64_t)row * kHc * kHc + kHc * i + 2 * h + 1] = P[i][h].y;
+    }
 }
 
 // The epilogue of the CTA's first nrows (<= 32) rows: one thread per row.

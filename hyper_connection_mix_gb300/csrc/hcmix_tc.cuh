@@ -27,12 +27,13 @@
 //     fixed tree, splits x into the limbs x0 (grid-aligned) and x1 = x - x0
 //     and stores both into TMEM A buffer k % 3 (x as fp32 in tf32x3 mode);
 //     the chunk's sum of squares goes to a shared-memory slot;
-//   * warps 12..19, the accumulate warps, two output groups of four: warp
-//     12 + 4 e + q reads outputs 12 e .. 12 e + 11 of the rows of quadrant q
-//     (4 x 12 D columns, one TMEM round trip), forms the chunk dots
-//     fl32(top + ((r1 + r2) + r3)), adds them into the slice totals (chunks
-//     in order, from zero) and stores them at the end of each unit to the
-//     workspace partials; group 0 does the same for the sums of squares;
+//   * warps 12..19, the accumulate warps, two halves of four (one per
+//     quadrant): half dh takes the units with i % 2 == dh, so that two
+//     units' reads are in flight at once.  They read D (two TMEM round trips
+//     of 4 x 12 columns), form the chunk dots fl32(top + ((r1 + r2) + r3)),
+//     add them into the slice totals (chunks in order, from zero), add the
+//     chunk's sum of squares likewise, and store the 24 + 1 slice totals per
+//     row to the workspace partials at the end of the unit;
 //   * the W operand: every CTA converts the fp32 W of its first two slices
 //     into the exact bf16 limbs (or the tf32x3 big / small parts) in shared
 //     memory during set-up (no separate pack kernel); the accumulate warps
@@ -86,7 +87,7 @@ constexpr int kNumMma = 3;  // MMA-issuing warps 0..2: chunk k to warp k % 3 (it
 constexpr int kXWarp = 3;   // the x producer (one lane)
 constexpr int kFirstTWarp = 4;   // transform warps 4..11
 constexpr int kNumTWarps = 8;
-constexpr int kFirstDWarp = 12;  // accumulate warps 12..19: warp 12 + 4 e + q, quadrant q, outputs 12 e..
+constexpr int kFirstDWarp = 12;  // accumulate warps 12..19: warp 12 + 4 dh + q, quadrant q, units i % 2 == dh
 constexpr int kNumDWarps = 8;
 constexpr int kFirstWorkWarp = 4;  // transform and accumulate warps: kFirstWorkWarp ..
 constexpr int kWarps = kFirstWorkWarp + kNumTWarps + kNumDWarps;
@@ -145,12 +146,13 @@ struct Bookkeeping {
   uint64_t a_empty[kNumA * 2];  // [k % 3 * 2 + k % 2]: the MMAs of chunk k are done
   uint64_t mma_ready[kNumMma];  // chunk k (issuer k % 3): A(k) written and D(k - 3) read
   uint64_t sq_full[kNumSq];
-  uint64_t d_full[kNumD];
+  uint64_t d_full[kNumD * 2];  // [b * 2 + (k / 4) % 2]: D buffer b holds chunk k, of accumulate half (k / 4) % 2
   uint64_t chunk_done[kNumSq];
   uint64_t w_full[kWBufs];
   uint64_t drain[kNumMma];
   uint64_t tail_bar[6];
   uint32_t tmem_base;
+  unsigned long long gbar_base;  // the grid barrier's counter before this CTA arrived, rounded down
   int abort;
   int never;  // stays 0: the abort flag of waits that must not be cut short
 };
@@ -170,8 +172,8 @@ static_assert(kNumTWarps == 2 * 4 && kFirstTWarp % 4 == 0 && kFirstDWarp % 4 == 
 static_assert(kNumMma == 3 && kNumA == 3 && kNumD == 3 && kNumTWarps == 8 && kNumDWarps == 8 &&
                   kXWarp < kFirstWorkWarp && kMmaWarp0 + kNumMma <= kFirstWorkWarp &&
                   (kXWarp < kMmaWarp0 || kXWarp >= kMmaWarp0 + kNumMma),
-              "issuer k % 3 owns A and D buffer k % 3; the transform warps are two halves, the "
-              "accumulate warps two output groups");
+              "issuer k % 3 owns A and D buffer k % 3; the transform warps are two halves by "
+              "chunk, the accumulate warps two halves by unit");
 
 // Parameters of one launch (passed by value as a __grid_constant__).
 struct TcParams {
@@ -181,7 +183,7 @@ struct TcParams {
   int64_t n_units;
   float* part;     // workspace partials [n_slices][25][Mpad]
   uint32_t* err;   // device error word
-  uint32_t* gbar_count, *gbar_gen;  // grid-barrier words (workspace header)
+  unsigned long long* gbar;  // the grid barrier's counter (workspace header)
   const float* w_src;  // fp32 W, converted in-kernel; null: limbs come by TMA
   int64_t w_stride;
   int tail;        // 0: partials only; 1: + mix / sq; 2: + epilogue (mix / sq optional)
@@ -482,23 +484,24 @@ __device__ __forceinline__ void fail(Bookkeeping& bk, uint32_t* err) {
   *reinterpret_cast<volatile int*>(&bk.abort) = 1;
 }
 
-// Grid-wide barrier on two words of the workspace header, called by one
-// thread per CTA after a CTA barrier that follows the CTA's stores.  The
-// arrival is a release at GPU scope (it publishes the CTA's stores); the last
-// CTA to arrive puts the count back to zero and moves the generation on with a
-// release, and the others wait, bounded, for the generation to move with
-// acquire loads.  Every CTA must be resident (cooperative launch).  Returns
-// false when the wait ran out.
-__device__ __forceinline__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t nblocks,
-                                             uint64_t limit_ns) {
-  const uint32_t g0 = sm100::ld_acquire_gpu(gen);  // before arriving: the last arrival moves it
-  if (sm100::atom_add_release_gpu(count, 1u) == nblocks - 1) {
-    *reinterpret_cast<volatile uint32_t*>(count) = 0u;
-    sm100::red_add_release_gpu(gen, 1u);  // also orders the reset before the next launch's arrivals
-    return true;
-  }
+// Grid-wide barrier on a monotonic 64-bit counter in the workspace header,
+// called by one thread per CTA after a CTA barrier that follows the CTA's
+// stores.  Every launch adds exactly kBarrierQuantum to it (each CTA 1, CTA 0
+// also the kBarrierQuantum - G of the CTAs the grid does not have), so at the
+// start of a launch it is a multiple of kBarrierQuantum, and any value a CTA
+// reads before its own arrival lies below the next multiple: `base` is that
+// value rounded down, and the barrier opens when the counter reaches base +
+// kBarrierQuantum.  The arrival is a release add at GPU scope (it publishes the
+// CTA's stores), the wait a bounded loop of acquire loads.  Every CTA must be
+// resident (cooperative launch).  Returns false when the wait ran out.
+constexpr unsigned long long kBarrierQuantum = 1024;  // above any grid size
+
+__device__ __forceinline__ bool grid_barrier(unsigned long long* counter, unsigned long long base,
+                                             int64_t b, int64_t nblocks, uint64_t limit_ns) {
+  sm100::red_add_release_gpu_u64(counter, b == 0 ? 1 + kBarrierQuantum - (unsigned long long)nblocks : 1);
+  const unsigned long long target = base + kBarrierQuantum;
   const uint64_t t0 = sm100::global_timer_ns();
-  for (uint32_t i = 0; sm100::ld_acquire_gpu(gen) == g0; ++i) {
+  for (uint32_t i = 0; sm100::ld_acquire_gpu_u64(counter) < target; ++i) {
     if ((i & 63u) == 63u && sm100::global_timer_ns() - t0 > limit_ns) return false;
   }
   return true;
@@ -718,18 +721,18 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         const uint64_t pol = l2_policy_evict_first();
         for (int L = 0; L < kXStages && L < n_loads; ++L) issue_x_load(L, pol);
       }
-      // mma_ready[k % 3]: the four transform warps of chunk k and the eight
-      // accumulate warps once they have read chunk k - 3 (for the first three
-      // chunks, those eight arrivals are made here)
+      // mma_ready[k % 3]: the four transform warps of chunk k and the four
+      // accumulate warps that have read chunk k - 3 (for the first three
+      // chunks, those four arrivals are made here)
       for (int c = 0; c < kNumMma; ++c) {
-        mbar_init(smem_u32(&bk.mma_ready[c]), 4 + kNumDWarps);
-        for (int q = 0; q < kNumDWarps; ++q) mbar_arrive(smem_u32(&bk.mma_ready[c]));
+        mbar_init(smem_u32(&bk.mma_ready[c]), 8);
+        for (int q = 0; q < 4; ++q) mbar_arrive(smem_u32(&bk.mma_ready[c]));
       }
       for (int a = 0; a < 2 * kNumA; ++a) mbar_init(smem_u32(&bk.a_empty[a]), 1);  // MMA commit
-      for (int d = 0; d < kNumD; ++d) mbar_init(smem_u32(&bk.d_full[d]), 1);  // MMA commit
+      for (int d = 0; d < 2 * kNumD; ++d) mbar_init(smem_u32(&bk.d_full[d]), 1);  // MMA commit
       for (int q = 0; q < kNumSq; ++q) {
         mbar_init(smem_u32(&bk.sq_full[q]), 4);     // the four transform warps of the chunk
-        mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the accumulate warps that read the sums
+        mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the four accumulate warps of the chunk
       }
       for (int w = 0; w < kWBufs; ++w) mbar_init(smem_u32(&bk.w_full[w]), 1);
       for (int g = 0; g < kNumMma; ++g) mbar_init(smem_u32(&bk.drain[g]), 1);
@@ -797,9 +800,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       const uint32_t d = tmem + kDCol0 + (uint32_t)t * kDCols<kTf32>;
       const uint64_t bdesc = smem_desc_sw128(wbuf(slot, c));
       if constexpr (kTf32)
-        mma_chunk_tf32x3(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t]));
+        mma_chunk_tf32x3(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t * 2 + (i & 1)]));
       else
-        mma_chunk_exact(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t]));
+        mma_chunk_exact(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t * 2 + (i & 1)]));
       umma_commit_warp(smem_u32(&bk.a_empty[t * 2 + (k & 1)]));
     }
     if (!ok && lane == 0) fail(bk, P.err);
@@ -911,15 +914,17 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
     if (!ok) fail(bk, P.err);
   } else if (warp >= kFirstDWarp && warp < kFirstDWarp + kNumDWarps) {
-    // ---------------- accumulate warps: warp 12 + 4 e + q reads, for the
-    // rows of quadrant q, the outputs 12 e .. 12 e + 11 of every chunk (its
-    // 4 x 12 D columns in one TMEM round trip), forms their chunk dots and
-    // adds them into the slice totals, chunks in order; group e = 0 also
-    // adds the sums of squares.  First all eight convert the second slice's
-    // W (when the CTA has one), which is not needed before the first unit is
-    // done.
-    const int e = (warp - kFirstDWarp) >> 2;
+    // ---------------- accumulate warps, two halves of four (one warp per
+    // quadrant each): half dh reads the units i with i % 2 == dh, all 24
+    // outputs, so that two units' chunk reads (TMEM round trips, adds,
+    // partial stores) are in flight at once.  First all eight convert the
+    // second slice's W (when the CTA has one), which is not needed before the
+    // first unit is done.
+    const int dh = (warp - kFirstDWarp) >> 2;
     const int dtid = threadIdx.x - kFirstDWarp * 32;  // 0..255
+    const int htid = dtid & 127;                       // within the half
+    if (dtid == 0 && P.tail != 0)  // (read before this CTA arrives; used after the teardown barrier)
+      bk.gbar_base = ld_relaxed_gpu_u64(P.gbar) / kBarrierQuantum * kBarrierQuantum;
     if (P.w_src != nullptr && n_sl >= 2) {
       convert_slice(1, dtid, kNumDWarps * 32, false);
       fence_proxy_async_smem();
@@ -928,20 +933,20 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         for (int c = 0; c < kChunksPerSlice; ++c)
           mbar_arrive(smem_u32(&bk.w_full[kChunksPerSlice + c]));
     }
-    // A CTA with more than two slices reuses the slots: once these warps
-    // have read the last chunk of slice j - 2, every MMA of that slice is
-    // complete, and they fill slice j's slot (j % 2) before reading on.
+    // A CTA with more than two slices reuses the slots: once a half has read
+    // the last chunk of slice j - 2, every MMA of that slice is complete, and
+    // that half fills slice j's slot (j % 2) before reading on.
     auto refill = [&](int jn) {
       const int slot = jn % kSlots;
       if (P.w_src != nullptr) {
-        convert_slice(jn, dtid, kNumDWarps * 32, false);
+        convert_slice(jn, htid, 4 * 32, false);
         fence_proxy_async_smem();
-        named_bar_sync(2, kNumDWarps * 32);
-        if (dtid == 0)
+        named_bar_sync(2 + dh, 4 * 32);
+        if (htid == 0)
           for (int c = 0; c < kChunksPerSlice; ++c)
             mbar_arrive(smem_u32(&bk.w_full[slot * kChunksPerSlice + c]));
       } else if constexpr (!kTf32) {
-        if (dtid == 0)
+        if (htid == 0)
           for (int c = 0; c < kChunksPerSlice; ++c)
             issue_w_load(slot, c, s_first + jn, l2_policy_evict_last());
       }
@@ -950,66 +955,74 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const uint64_t keep = l2_policy_evict_last();  // the tail reads the partials next
-    constexpr int kOut = kMix / 2;  // outputs per group
+    // the parity of the next phase this half waits for on d_full[b][dh]
+    // (this half waits for every phase of its three barriers, in order)
+    uint32_t dpar = 0;
     bool ok = true;
-    for (int i = 0; ok && i < n; ++i) {
-      float2 acc[kOut / 2];
+    for (int i = dh; ok && i < n; i += 2) {
+      float2 acc[kMix / 2];
 #pragma unroll
-      for (int j = 0; j < kOut / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+      for (int j = 0; j < kMix / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
       float sqs = 0.0f;
       for (int c = 0; c < kChunksPerSlice; ++c) {
-        const int k = kChunksPerSlice * i + c;
-        // D of chunk k complete (and, for group 0, the chunk's sum of
-        // squares in its slot)
-        bool got = mbar_wait(smem_u32(&bk.d_full[k % kNumD]), (uint32_t)(k / kNumD) & 1u,
-                             abort_flag, kWaitLimitNs);
-        if (e == 0)
-          got = got && mbar_wait(smem_u32(&bk.sq_full[k % kNumSq]), (uint32_t)(k / kNumSq) & 1u,
-                                 abort_flag, kWaitLimitNs);
+        const int k = kChunksPerSlice * i + c, b = k % kNumD;
+        // D of chunk k complete, and the chunk's sum of squares in its slot
+        // (slot k % 8 = 4 dh + c: only this half reads it)
+        bool got = mbar_wait(smem_u32(&bk.d_full[b * 2 + dh]), (dpar >> b) & 1u, abort_flag,
+                             kWaitLimitNs);
+        dpar ^= 1u << b;
+        got = got && mbar_wait(smem_u32(&bk.sq_full[k % kNumSq]), (uint32_t)(k / kNumSq) & 1u,
+                               abort_flag, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d_col = tmem + kDCol0 + (uint32_t)(k % kNumD) * kDCols<kTf32>;
-        const float tsq = e == 0 ? sq_buf[(k % kNumSq) * kTileM + row] : 0.0f;
+        const uint32_t d_col = tmem + kDCol0 + (uint32_t)b * kDCols<kTf32>;
+        const float tsq = sq_buf[(k % kNumSq) * kTileM + row];
         if constexpr (kTf32) {
-          // D's first 24 columns are the chunk dots
-          uint32_t dv[kOut];
-          tmem_ld8(lanes | (d_col + kOut * e), dv);
-          tmem_ld4(lanes | (d_col + kOut * e + 8), dv + 8);
+          uint32_t dv[kMix];
+          tmem_ld16(lanes | d_col, dv);
+          tmem_ld8(lanes | (d_col + 16), dv + 16);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            if (e == 0) mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
-            mbar_arrive(smem_u32(&bk.mma_ready[k % kNumMma]));  // D buffer free for chunk k + 3
+            mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
+            mbar_arrive(smem_u32(&bk.mma_ready[b]));  // D buffer b free for chunk k + 3
           }
 #pragma unroll
-          for (int j = 0; j < kOut / 2; ++j)
+          for (int j = 0; j < kMix / 2; ++j)
             acc[j] = __fadd2_rn(acc[j], make_float2(__uint_as_float(dv[2 * j]),
                                                     __uint_as_float(dv[2 * j + 1])));
         } else {
           // D = [top | r1 | r2 | r3] (24 columns each); chunk dot = top + ((r1
-          // + r2) + r3), for this group's 12 outputs of each
-          uint32_t dv[4][kOut];
+          // + r2) + r3).  Outputs 0..11 first, then 12..23 (two TMEM round
+          // trips keep the registers within the budget); the D buffer is
+          // handed back once the second round is in registers.
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            tmem_ld8(lanes | (d_col + kMix * g + kOut * e), dv[g]);
-            tmem_ld4(lanes | (d_col + kMix * g + kOut * e + 8), dv[g] + 8);
-          }
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if (e == 0) mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
-            mbar_arrive(smem_u32(&bk.mma_ready[k % kNumMma]));  // D buffer free for chunk k + 3
-          }
+          for (int r = 0; r < 2; ++r) {
+            uint32_t dv[4][12];
 #pragma unroll
-          for (int j = 0; j < kOut / 2; ++j) {
-            const float2 top = make_float2(__uint_as_float(dv[0][2 * j]), __uint_as_float(dv[0][2 * j + 1]));
-            const float2 u = make_float2(__uint_as_float(dv[1][2 * j]), __uint_as_float(dv[1][2 * j + 1]));
-            const float2 v = make_float2(__uint_as_float(dv[2][2 * j]), __uint_as_float(dv[2][2 * j + 1]));
-            const float2 w = make_float2(__uint_as_float(dv[3][2 * j]), __uint_as_float(dv[3][2 * j + 1]));
-            acc[j] = __fadd2_rn(acc[j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
+            for (int g = 0; g < 4; ++g) {
+              tmem_ld8(lanes | (d_col + kMix * g + 12 * r), dv[g]);
+              tmem_ld4(lanes | (d_col + kMix * g + 12 * r + 8), dv[g] + 8);
+            }
+            tmem_wait_ld();
+            if (r == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
+                mbar_arrive(smem_u32(&bk.mma_ready[b]));  // D buffer b free for chunk k + 3
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 6; ++j) {
+              const float2 top = make_float2(__uint_as_float(dv[0][2 * j]), __uint_as_float(dv[0][2 * j + 1]));
+              const float2 u = make_float2(__uint_as_float(dv[1][2 * j]), __uint_as_float(dv[1][2 * j + 1]));
+              const float2 v = make_float2(__uint_as_float(dv[2][2 * j]), __uint_as_float(dv[2][2 * j + 1]));
+              const float2 w = make_float2(__uint_as_float(dv[3][2 * j]), __uint_as_float(dv[3][2 * j + 1]));
+              acc[6 * r + j] = __fadd2_rn(acc[6 * r + j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
+            }
           }
         }
         sqs = __fadd_rn(sqs, tsq);
@@ -1017,11 +1030,11 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       if (!ok) break;
       float* p = P.part + part_index(unit_tile(i) * kTileM + row, unit_slice(i), 0, P.n_slices);
 #pragma unroll
-      for (int j = 0; j < kOut / 2; ++j) {
-        stg_f32_hint(p + 8 * (kOut * e + 2 * j), acc[j].x, keep);
-        stg_f32_hint(p + 8 * (kOut * e + 2 * j + 1), acc[j].y, keep);
+      for (int j = 0; j < kMix / 2; ++j) {
+        stg_f32_hint(p + 8 * (2 * j), acc[j].x, keep);
+        stg_f32_hint(p + 8 * (2 * j + 1), acc[j].y, keep);
       }
-      if (e == 0) stg_f32_hint(p + 8 * kMix, sqs, keep);
+      stg_f32_hint(p + 8 * kMix, sqs, keep);
       // the last unit of slice j done: slice j + 2 (if any) may take its slot
       const int j = unit_slice(i) - s_first;
       if (j + kSlots < n_sl && (i == n - 1 || unit_slice(i + 1) != unit_slice(i)))
@@ -1051,7 +1064,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   // adds the slices of its rows in slice order and runs the epilogue; the x
   // and W buffers are idle now and hold the tail's copies
   if (threadIdx.x == 0 &&
-      !grid_barrier(P.gbar_count, P.gbar_gen, (uint32_t)G, kWaitLimitNs))
+      !grid_barrier(P.gbar, bk.gbar_base, b, G, kWaitLimitNs))
     record_device_error(P.err, kDevWaitTimeout);
   cta_barrier();
   tc_tail(P, smem, bk.tail_bar, never, b, G);
@@ -1205,8 +1218,7 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
   P.n_units = (int64_t)P.n_tiles * P.n_slices;
   P.part = part;
   P.err = header;
-  P.gbar_count = header + 16;
-  P.gbar_gen = header + 32;
+  P.gbar = reinterpret_cast<unsigned long long*>(header + 16);
   P.w_src = W;
   P.w_stride = w_stride;
   P.tail = t.tail;

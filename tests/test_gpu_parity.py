@@ -220,6 +220,21 @@ def test_sinkhorn_iteration_counts(path):
     check_all(x, W, sc, bs, path, "hc_eps", hc_eps=0.01)
 
 
+def test_sinkhorn_row_below_the_normal_range(path):
+    """A comb row whose exponentials are subnormal (logits near -89.8 with x = 0,
+    so logit = hc_base): its sums fall below the normal range, where a
+    reciprocal overflows; the epilogue then divides by the sums, as the oracle
+    does, and the results stay within the tolerance."""
+    K = 1024
+    x = np.zeros((12, K), np.uint16)
+    bs = hi.make_base()
+    bs[8:12] = np.float32(-89.8)
+    bs[12:16] = np.float32(-89.3)
+    got = run(x, hi.make_w(K=K), hi.make_scale(), bs, path)
+    assert all(np.isfinite(g).all() for g in got[:3])
+    check_all(x, hi.make_w(K=K), hi.make_scale(), bs, path, "subnormal comb row")
+
+
 def test_empty_batch_is_a_no_op(path):
     x = torch.zeros(0, 256, dtype=torch.bfloat16, device="cuda")
     W = torch.zeros(24, 256, dtype=torch.float32, device="cuda")

@@ -1,7 +1,8 @@
 """The tensor-core kernel's hand-off protocol, checked on the CPU.
 
-The kernel's roles (the x producer, two halves of four transform warps, three
-MMA issuers, two output groups of four accumulate warps, the W-slot refills) hand chunks to each other through mbarriers whose waits only test the
+The kernel's roles (the x producer, two halves of four transform warps by
+chunk, three MMA issuers, two halves of four accumulate warps by unit, the
+W-slot refills) hand chunks to each other through mbarriers whose waits only test the
 parity of the phase they want.  Such a wait is sound only when the waiter
 already knows the phase before it complete; otherwise it cannot tell phase
 p - 2 from phase p and returns early.  This module restates, role by role, the
@@ -49,15 +50,16 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     nck, nld = 4 * n, 2 * n
     mk = lambda p, c, m: [Bar(c, f"{p}{i}") for i in range(m)]
     full_x, empty_x = mk("full_x", 1, X_STAGES), mk("empty_x", 8, X_STAGES)
-    # mma_ready[k % 3]: the four transform warps of chunk k and the eight
-    # accumulate warps once they have read chunk k - 3 (made at set-up for k < 3)
-    mma_ready = mk("mma_ready", 12, N_MMA)
+    # mma_ready[k % 3]: the four transform warps of chunk k and the four
+    # accumulate warps that have read chunk k - 3 (made at set-up for k < 3)
+    mma_ready = mk("mma_ready", 8, N_MMA)
     for b in mma_ready:
-        for _ in range(8):
+        for _ in range(4):
             b.arrive()
     a_empty = mk("a_empty", 1, 2 * N_A)  # [k % 3 * 2 + k % 2]: chunk k's MMAs done
     sq_full, chunk_done = mk("sq_full", 4, N_SQ), mk("chunk_done", 4, N_SQ)
-    d_full, w_full = mk("d_full", 1, N_D), mk("w_full", 1, 4 * SLOTS)
+    # d_full[b * 2 + h]: D buffer b holds a chunk of accumulate half h
+    d_full, w_full = mk("d_full", 1, 2 * N_D), mk("w_full", 1, 4 * SLOTS)
     dconv = Bar(8, "dconv")
     errors, pipe, tma = [], [], []
     # progress, for the buffer checks
@@ -65,7 +67,6 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     mma_done = set()            # chunks whose MMAs completed
     d_read = [0] * nck          # accumulate warps that have read D of chunk k
     sq_read = [0] * nck         # accumulate warps that have read the sum of squares of chunk k
-    refill_bar = Bar(8, "refill")
     slice_done = set()          # slices whose every MMA completed (W slot free)
 
     def wait(bar, phase, who):
@@ -116,45 +117,40 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
             # a W barrier: its earlier fill always completed before any issuer
             # waits for the next, so several issuers may wait on it
             yield from wait(w_full[(j % SLOTS) * 4 + c], j // SLOTS, f"I{t} k{k} W")
-            check(k < N_D or d_read[k - N_D] == 8, f"D buffer of chunk {k} over an unread one")
+            check(k < N_D or d_read[k - N_D] == 4, f"D buffer of chunk {k} over an unread one")
             check(j < SLOTS or (s - SLOTS) in slice_done, f"chunk {k} reads a W slot being refilled")
             yield None
-            pipe.append(k)
+            pipe.append((k, (k % N_D) * 2 + i % 2))
 
-    def accumulate(e, q):  # outputs 12 e.. of quadrant q
+    def accumulate(dh, q):  # the units i with i % 2 == dh, quadrant q
         if not packed and n_sl >= 2:  # the second slice, converted during set-up by all eight
             yield None
             dconv.arrive()
             while dconv.phase == 0:
                 yield (dconv, 0)
-            if e == 0 and q == 0:
+            if dh == 0 and q == 0:
                 for c in range(4):
                     w_full[4 + c].arrive()
-        for i in range(n):
+        seen = [0] * N_D  # phases of d_full[b * 2 + dh] waited for so far
+        for i in range(dh, n, 2):
             for c in range(4):
                 k = 4 * i + c
-                dbar = k % N_D if PLANTED != "d_full_by_issuer" else c % N_D
-                yield from wait(d_full[dbar], k // N_D, f"D{e}{q} k{k}")
-                if e == 0:
-                    yield from wait(sq_full[k % N_SQ], k // N_SQ, f"D{e}{q} k{k} sq")
+                b = k % N_D
+                dbar = b * 2 + dh if PLANTED != "d_full_by_buffer" else b * 2
+                yield from wait(d_full[dbar], seen[b], f"D{dh}{q} k{k}")
+                seen[b] += 1
+                yield from wait(sq_full[k % N_SQ], k // N_SQ, f"D{dh}{q} k{k} sq")
                 check(k in mma_done, f"D of chunk {k} read before its MMAs completed")
                 yield None
                 d_read[k] += 1
-                if e == 0:
-                    sq_read[k] += 1
-                    chunk_done[k % N_SQ].arrive()
-                mma_ready[k % N_MMA].arrive()  # D buffer free for chunk k + 3
+                sq_read[k] += 1
+                chunk_done[k % N_SQ].arrive()
+                mma_ready[b].arrive()  # D buffer b free for chunk k + 3
             j = sl[i] - s_first
-            if j + SLOTS < n_sl and (i == n - 1 or sl[i + 1] != sl[i]):
-                # refill by all eight (a named barrier), then one arrival
-                target = refill_bar.phase + 1  # the phase this arrival belongs to completes
-                refill_bar.arrive()
-                while refill_bar.phase < target:
-                    yield (refill_bar, (target - 1) & 1)
-                if e == 0 and q == 0:
-                    slice_done.add(sl[i])
-                    for c in range(4):  # slice j + 2 into slot j % 2
-                        w_full[((j + SLOTS) % SLOTS) * 4 + c].arrive()
+            if j + SLOTS < n_sl and (i == n - 1 or sl[i + 1] != sl[i]) and q == 0:
+                slice_done.add(sl[i])
+                for c in range(4):  # refill: slice j + 2 into slot j % 2
+                    w_full[((j + SLOTS) % SLOTS) * 4 + c].arrive()
 
     for c in range(4 * min(SLOTS, n_sl) if packed else 4):
         w_full[c].arrive()  # set-up: the first slice (and the second, prepacked)
@@ -163,7 +159,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     roles = {"x": x_producer()}
     roles.update({f"I{g}": issuer(g) for g in range(N_MMA)})
     roles.update({f"T{h}{q}": transform(h, q) for h in (0, 1) for q in range(4)})
-    roles.update({f"D{e}{q}": accumulate(e, q) for e in (0, 1) for q in range(4)})
+    roles.update({f"D{h}{q}": accumulate(h, q) for h in (0, 1) for q in range(4)})
     state = {r: None for r in roles}
     done = set()
     while True:
@@ -171,9 +167,9 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                  (state[r] is None or (state[r][0].phase & 1) != state[r][1])]
         if (pipe or tma) and (not ready or rnd.random() < 0.3):
             if pipe and (not tma or rnd.random() < 0.5):
-                k = pipe.pop(0)  # the tensor pipe completes MMAs in issue order
+                k, dbar = pipe.pop(0)  # the tensor pipe completes MMAs in issue order
                 mma_done.add(k)
-                d_full[k % N_D].arrive()
+                d_full[dbar].arrive()
                 a_empty[(k % N_A) * 2 + k % 2].arrive()
             else:
                 st, _ = tma.pop(rnd.randrange(len(tma)))
@@ -216,12 +212,12 @@ def test_protocol_sound_and_deadlock_free(M, K):
                 assert not errs, f"M={M} K={K} units {ub}+{n} seed {seed}: {errs[:3]}"
 
 
-@pytest.mark.parametrize("mistake", ["own_half_a_empty", "d_full_by_issuer"])
+@pytest.mark.parametrize("mistake", ["own_half_a_empty", "d_full_by_buffer"])
 def test_model_catches_planted_mistakes(mistake):
     """The checks have teeth: a transform half that waits for its own previous
     chunk on A buffer k % 3 (instead of chunk k - 3, the other half's), or
-    accumulate warps that wait on the D barrier of the issuer rather than of
-    the buffer, are reported (an early return, a buffer rewritten too soon, or
+    accumulate halves that share one D barrier per buffer (each then sees only
+    some of its phases), are reported (an early return, a buffer rewritten too soon, or
     the deadlock they lead to)."""
     global PLANTED
     PLANTED = mistake
