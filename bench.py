@@ -10,9 +10,14 @@ Our arm prints one JSON line with:
   value      device-timed us per call (CUDA events around exactly K calls,
              replayed from CUDA graphs of 10 calls and one remainder graph;
              with N ranks, max elapsed / (K * N));
-  roofline   the contraction kernel timed alone with CUDA events on its stream,
-             algorithmic bytes (x once + W once) / average duration, against the
-             measured HBM copy bandwidth;
+  roofline   the dominant kernel with CUDA events on its stream: on the
+             tensor-core path the whole call is one launch of hcmix_tc_kernel
+             (contraction, in-kernel W conversion, grid barrier, slice-ordered
+             reduce and epilogue), so its duration is the call's; on the
+             two-launch paths the contraction kernel is timed alone.
+             Algorithmic bytes (x once + W once) / average duration, against
+             the measured HBM copy bandwidth; the contraction phase alone is
+             reported beside it;
   e2e        the same metric through the C ABI with host buffers: every step
              copies x, W, hc_scale, hc_base from pinned host memory and reads
              pre, post, comb back; x goes in four row blocks, each block's call
@@ -70,6 +75,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="time the other workloads (one JSON line each) instead of the headline")
+    ap.add_argument("--profile-rows", type=int, default=0,
+                    help="no timing: four hc_mix_fused calls of this many rows (the command the "
+                         "committed ncu summaries capture)")
     ap.add_argument("--protocols", action="store_true",
                     help="the 4096-row call with rotated x buffers and with a scrubbed L2, and "
                          "the oracle on one thread and on every host core (one JSON line each)")
@@ -282,7 +290,10 @@ def run_ours(args, rank, world, local):
         call()
         torch.cuda.synchronize()
         graphs = calls_graphs(call, stream)
-    launches_per_call = 2 if path == "simt" else 3
+    # tc / tc_tf32x3: one cooperative launch per call; simt / tc_staged: the
+    # contraction, then the reduce + epilogue kernel
+    single_launch = path in ("tc", "tc_tf32x3")
+    launches_per_call = 1 if single_launch else 2
 
     # ---- device-timed value: exactly K calls, as CUDA-graph replays of
     # GRAPH_CALLS calls each (and one remainder graph)
@@ -305,8 +316,8 @@ def run_ours(args, rank, world, local):
     us_call = ms * 1e3 / (args.steps * world)
     alg_bytes = traffic.algorithmic_bytes(M, K)
 
-    # ---- dominant kernels alone: the contraction (W-limb pack + contraction),
-    # replayed from CUDA graphs so that host launch cost is not timed
+    # ---- the contraction phase alone (tail = 0: no grid barrier, reduce or
+    # epilogue), replayed from CUDA graphs so that host launch cost is not timed
     n_k = max(3, min(args.steps, 2000))
     with torch.cuda.stream(stream):
         contract = lambda: binding.hc_mix_contract(x, W, ws, stream=stream, path=path)
@@ -320,10 +331,15 @@ def run_ours(args, rank, world, local):
         replay_calls(kgraphs, n_k)
         c1.record(stream)
         c1.synchronize()
-    k_us = c0.elapsed_time(c1) * 1e3 / n_k
+    contract_us = c0.elapsed_time(c1) * 1e3 / n_k
     peak, peak_kind = measured_peaks()
+    if single_launch:  # the call is one launch of the kernel: its duration is the call's
+        k_us = us_call * world
+        kernel_name = "hcmix_tc_kernel"
+    else:
+        k_us = contract_us
+        kernel_name = "hcmix_simt_slice_kernel" if path == "simt" else "hcmix_tc_kernel"
     achieved = alg_bytes / (k_us * 1e-6) / 1e9
-    kernel_name = "hcmix_simt_slice_kernel" if path == "simt" else "hcmix_tc_kernel"
 
     # ---- end to end through the C ABI with host buffers
     x_pin = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -412,8 +428,11 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": kernel_name, "kernel_us": k_us,
+                     "launches_per_call": launches_per_call,
                      "traffic": profiled_traffic(kernel_name),
-                     "algorithmic_bytes": alg_bytes},
+                     "algorithmic_bytes": alg_bytes,
+                     "contraction_phase_us": contract_us,
+                     "contraction_phase_frac": alg_bytes / (contract_us * 1e-6) / 1e9 / peak},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -675,11 +694,40 @@ def run_protocols(args):
                       "extrapolated": "one call on one thread, times 86"}), flush=True)
 
 
+def run_profile(args):
+    """Four hc_mix_fused calls of --profile-rows rows (seeded inputs), then a
+    check of the device status word; for ncu captures of one launch."""
+    import numpy as np
+    import torch
+
+    import hcmix_inputs as hi
+    from hyper_connection_mix_gb300 import binding
+
+    M = args.profile_rows
+    path = args.path if args.path != "auto" else binding.hc_mix_auto_path(M)
+    x = torch.from_numpy(hi.make_x(M).view(np.int16)).view(torch.bfloat16).cuda()
+    W, sc, bs = (torch.from_numpy(a).cuda() for a in (hi.make_w(), hi.make_scale(), hi.make_base()))
+    ws = binding.alloc_workspace(M, K_COLS)
+    out = (torch.empty(M, 4, device="cuda"), torch.empty(M, 4, device="cuda"),
+           torch.empty(M, 4, 4, device="cuda"))
+    for _ in range(4):
+        binding.hc_mix_fused(x, W, sc, bs, ITERS, RMS_EPS, HC_EPS, out=out, workspace=ws, path=path)
+    torch.cuda.synchronize()
+    status = binding.hc_mix_device_status(ws)
+    print(json.dumps({"profile_rows": M, "path": path, "device_status": status}), flush=True)
+    if status != 0:
+        raise SystemExit(1)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     rank, world, local = dist_env()
+    if args.profile_rows:
+        if rank == 0:
+            run_profile(args)
+        return
     if args.sweep:
         if rank == 0:
             run_sweep(args)
