@@ -663,10 +663,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 0, full, pol);
   };
   // the fp32 W of slice index j (slot j % 2), converted by the `nthreads`
-  // threads numbered `tid` from 0, all of a thread's W loads in flight at once
-  // (with `zero`, the zero rows of the exact-mode W buffers are written while
-  // they are on their way)
-  auto convert_slice = [&](int j, int tid, int nthreads, bool zero) {
+  // threads numbered `tid` from 0, a batch of each thread's W loads in flight
+  // at once
+  auto convert_slice = [&](int j, int tid, int nthreads) {
     constexpr int kTasks = kMix * kChunksPerSlice;  // (output, chunk) pairs, 16 lanes each
     const int groups = nthreads / 16, sub = tid & 15;
     constexpr int kMaxRounds = 12;  // 96 tasks over at least 8 groups
@@ -683,15 +682,6 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
           wv[q] = *reinterpret_cast<const float4*>(
               P.w_src + (int64_t)(task / kChunksPerSlice) * P.w_stride +
               (int64_t)(s_first + j) * kSlice + (task % kChunksPerSlice) * kChunk + 4 * sub);
-      }
-      if constexpr (!kTf32) {
-        if (zero && q0 == 0) {
-          constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
-          for (int idx = tid; idx < kWBufs * kUnits; idx += nthreads) {
-            const int w = idx / kUnits, u = idx % kUnits;
-            sts128(w_base + (uint32_t)w * MD::kBBytes + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
-          }
-        }
       }
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {  // uniform trip count: the shuffles need whole warps
@@ -752,10 +742,11 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     tmem_alloc(smem_u32(&bk.tmem_base), kTmemCols);
     tmem_relinquish();
   } else if (warp >= kFirstWorkWarp) {
+    // the zero rows of the exact-mode W buffers (the fp32 W itself is
+    // converted by the accumulate warps after set-up, while the transform
+    // warps already work on the first x loads)
     const int tid = threadIdx.x - kFirstWorkWarp * 32, nthr = kThreads - kFirstWorkWarp * 32;
-    if (P.w_src != nullptr) {
-      convert_slice(0, tid, nthr, true);
-    } else if constexpr (!kTf32) {  // prepacked limbs: only the zero rows
+    if constexpr (!kTf32) {
       constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
       for (int idx = tid; idx < kWBufs * kUnits; idx += nthr) {
         const int w = idx / kUnits, u = idx % kUnits;
@@ -767,8 +758,6 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   tc_fence_before();
   cta_barrier();
   tc_fence_after();
-  if (threadIdx.x == kFirstWorkWarp * 32 && P.w_src != nullptr)  // the first slice is in place
-    for (int c = 0; c < kChunksPerSlice; ++c) mbar_arrive(smem_u32(&bk.w_full[c]));
   const uint32_t tmem = bk.tmem_base;
   const volatile int* abort_flag = &bk.abort;
   const volatile int* never = &bk.never;
@@ -917,21 +906,24 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // ---------------- accumulate warps, two halves of four (one warp per
     // quadrant each): half dh reads the units i with i % 2 == dh, all 24
     // outputs, so that two units' chunk reads (TMEM round trips, adds,
-    // partial stores) are in flight at once.  First all eight convert the
-    // second slice's W (when the CTA has one), which is not needed before the
-    // first unit is done.
+    // partial stores) are in flight at once.  First all eight convert the W
+    // of the CTA's first two slices, which the MMAs need before any D is
+    // ready to read.
     const int dh = (warp - kFirstDWarp) >> 2;
     const int dtid = threadIdx.x - kFirstDWarp * 32;  // 0..255
     const int htid = dtid & 127;                       // within the half
     if (dtid == 0 && P.tail != 0)  // (read before this CTA arrives; used after the teardown barrier)
       bk.gbar_base = ld_relaxed_gpu_u64(P.gbar) / kBarrierQuantum * kBarrierQuantum;
-    if (P.w_src != nullptr && n_sl >= 2) {
-      convert_slice(1, dtid, kNumDWarps * 32, false);
-      fence_proxy_async_smem();
-      named_bar_sync(1, kNumDWarps * 32);
-      if (dtid == 0)
-        for (int c = 0; c < kChunksPerSlice; ++c)
-          mbar_arrive(smem_u32(&bk.w_full[kChunksPerSlice + c]));
+    if (P.w_src != nullptr) {
+      // the first two slices' W (the MMAs of each wait for its w_full)
+      for (int j = 0; j < kSlots && j < n_sl; ++j) {
+        convert_slice(j, dtid, kNumDWarps * 32);
+        fence_proxy_async_smem();
+        named_bar_sync(1, kNumDWarps * 32);
+        if (dtid == 0)
+          for (int c = 0; c < kChunksPerSlice; ++c)
+            mbar_arrive(smem_u32(&bk.w_full[j * kChunksPerSlice + c]));
+      }
     }
     // A CTA with more than two slices reuses the slots: once a half has read
     // the last chunk of slice j - 2, every MMA of that slice is complete, and
@@ -939,7 +931,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     auto refill = [&](int jn) {
       const int slot = jn % kSlots;
       if (P.w_src != nullptr) {
-        convert_slice(jn, htid, 4 * 32, false);
+        convert_slice(jn, htid, 4 * 32);
         fence_proxy_async_smem();
         named_bar_sync(2 + dh, 4 * 32);
         if (htid == 0)

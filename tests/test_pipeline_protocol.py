@@ -123,14 +123,15 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
             pipe.append((k, (k % N_D) * 2 + i % 2))
 
     def accumulate(dh, q):  # the units i with i % 2 == dh, quadrant q
-        if not packed and n_sl >= 2:  # the second slice, converted during set-up by all eight
-            yield None
-            dconv.arrive()
-            while dconv.phase == 0:
-                yield (dconv, 0)
-            if dh == 0 and q == 0:
-                for c in range(4):
-                    w_full[4 + c].arrive()
+        if not packed:  # the first two slices' W, converted by all eight first
+            for j in range(min(SLOTS, n_sl)):
+                yield None
+                dconv.arrive()
+                while dconv.phase <= j:
+                    yield (dconv, j & 1)
+                if dh == 0 and q == 0:
+                    for c in range(4):
+                        w_full[4 * j + c].arrive()
         seen = [0] * N_D  # phases of d_full[b * 2 + dh] waited for so far
         for i in range(dh, n, 2):
             for c in range(4):
@@ -152,8 +153,9 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                 for c in range(4):  # refill: slice j + 2 into slot j % 2
                     w_full[((j + SLOTS) % SLOTS) * 4 + c].arrive()
 
-    for c in range(4 * min(SLOTS, n_sl) if packed else 4):
-        w_full[c].arrive()  # set-up: the first slice (and the second, prepacked)
+    if packed:
+        for c in range(4 * min(SLOTS, n_sl)):
+            w_full[c].arrive()  # set-up: TMA loads of the first two slices' limbs
     for L in range(min(X_STAGES, nld)):  # set-up: the first x loads
         issue_load(L)
     roles = {"x": x_producer()}
