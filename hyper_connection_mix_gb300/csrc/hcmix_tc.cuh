@@ -77,23 +77,24 @@ namespace tc {
 
 constexpr int kXStages = 3;        // x stages in flight
 constexpr int kChunksPerStage = 2;  // an x stage holds two chunks of a tile (one 32 KB load)
-constexpr int kNumA = 3;   // TMEM A buffers: chunk k uses A buffer k % 3
+constexpr int kNumA = 3;   // TMEM A buffers: chunk k uses A buffer k % 3 (transform third k % 3)
 constexpr int kNumD = 3;   // TMEM D buffers: chunk k uses D buffer k % 3
-constexpr int kNumSq = 8;  // sum-of-squares slots (shared memory)
+constexpr int kNumSq = 6;  // sum-of-squares slots (shared memory): chunk k uses slot k % 6
 constexpr int kSlots = 2;  // W slots: a CTA's consecutive slices alternate between them
 constexpr int kWBufs = kSlots * kChunksPerSlice;
 constexpr int kMmaWarp0 = 0, kTmemWarp = 1;
 constexpr int kNumMma = 3;  // MMA-issuing warps 0..2: chunk k to warp k % 3 (its A and D buffers)
 constexpr int kXWarp = 3;   // the x producer (one lane)
-constexpr int kFirstTWarp = 4;   // transform warps 4..11
-constexpr int kNumTWarps = 8;
-constexpr int kFirstDWarp = 12;  // accumulate warps 12..19: warp 12 + 4 dh + q, quadrant q, units i % 2 == dh
+constexpr int kFirstTWarp = 4;   // transform warps 4..15: three thirds of four, chunks k % 3
+constexpr int kNumTWarps = 12;
+constexpr int kFirstDWarp = 16;  // accumulate warps 16..23: warp 16 + 4 dh + q, quadrant q, units i % 2 == dh
 constexpr int kNumDWarps = 8;
 constexpr int kFirstWorkWarp = 4;  // transform and accumulate warps: kFirstWorkWarp ..
 constexpr int kWarps = kFirstWorkWarp + kNumTWarps + kNumDWarps;
 constexpr int kThreads = kWarps * 32;
 // registers per thread: the register file of a sub-partition (16K) over its warps
 constexpr int kMaxRegs = (16384 / (((kWarps + 3) / 4) * 32)) / 8 * 8;
+constexpr int kDRounds = kMaxRegs >= 96 ? 2 : 3;  // TMEM round trips per chunk for D
 constexpr int kTileM = 128;
 constexpr uint32_t kRowBytes = 128;                           // 64 bf16 per smem row
 constexpr uint32_t kXChunkBytes = kTileM * kRowBytes;         // one chunk of a tile
@@ -143,11 +144,11 @@ constexpr size_t kSmemBytes = kBkOff<kTf32> + 1024 + 1024;  // bookkeeping + bas
 struct Bookkeeping {
   uint64_t full_x[kXStages];
   uint64_t empty_x[kXStages];
-  uint64_t a_empty[kNumA * 2];  // [k % 3 * 2 + k % 2]: the MMAs of chunk k are done
+  uint64_t a_empty[kNumA];  // [k % 3]: the MMAs of chunk k are done (A buffer free)
   uint64_t mma_ready[kNumMma];  // chunk k (issuer k % 3): A(k) written and D(k - 3) read
-  uint64_t sq_full[kNumSq];
+  uint64_t sq_full[kNumSq * 2];     // [k % 6 * 2 + (k / 4) % 2]: chunk k's sum of squares is in its slot
   uint64_t d_full[kNumD * 2];  // [b * 2 + (k / 4) % 2]: D buffer b holds chunk k, of accumulate half (k / 4) % 2
-  uint64_t chunk_done[kNumSq];
+  uint64_t chunk_done[kNumSq * 2];  // [k % 6 * 2 + (k / 4) % 2]: the accumulate half has read it
   uint64_t w_full[kWBufs];
   uint64_t drain[kNumMma];
   uint64_t tail_bar[6];
@@ -164,16 +165,18 @@ static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of o
 static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynamic shared memory");
 static_assert(Mode<false>::kBBytes % 1024 == 0 && Mode<true>::kBlockBytes % 1024 == 0,
               "W buffers keep the 1 KB swizzle atoms aligned");
-static_assert(kNumTWarps == 2 * 4 && kFirstTWarp % 4 == 0 && kFirstDWarp % 4 == 0 &&
+static_assert(kNumTWarps == 3 * 4 && kFirstTWarp % 4 == 0 && kFirstDWarp % 4 == 0 &&
                   kFirstTWarp >= kFirstWorkWarp && kFirstDWarp >= kFirstWorkWarp &&
                   kFirstTWarp + kNumTWarps <= kWarps && kFirstDWarp + kNumDWarps <= kWarps &&
                   (kFirstTWarp + kNumTWarps <= kFirstDWarp || kFirstDWarp + kNumDWarps <= kFirstTWarp),
               "warp roles");
-static_assert(kNumMma == 3 && kNumA == 3 && kNumD == 3 && kNumTWarps == 8 && kNumDWarps == 8 &&
+static_assert(kNumMma == 3 && kNumA == 3 && kNumD == 3 && kNumTWarps == 12 && kNumDWarps == 8 &&
+                  kNumSq % 3 == 0 && kXStages == 3 && kChunksPerStage == 2 &&
                   kXWarp < kFirstWorkWarp && kMmaWarp0 + kNumMma <= kFirstWorkWarp &&
                   (kXWarp < kMmaWarp0 || kXWarp >= kMmaWarp0 + kNumMma),
-              "issuer k % 3 owns A and D buffer k % 3; the transform warps are two halves by "
-              "chunk, the accumulate warps two halves by unit");
+              "issuer k % 3 and transform third k % 3 own A buffer k % 3 (so a stage slot "
+              "always holds the chunks of the same two thirds); the accumulate warps are two "
+              "halves by unit");
 
 // Parameters of one launch (passed by value as a __grid_constant__).
 struct TcParams {
@@ -704,7 +707,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     if (lane == 0) {
       for (int s = 0; s < kXStages; ++s) {
         mbar_init(smem_u32(&bk.full_x[s]), 1);
-        mbar_init(smem_u32(&bk.empty_x[s]), kNumTWarps);
+        mbar_init(smem_u32(&bk.empty_x[s]), kChunksPerStage * 4);  // the four transform warps of each chunk
       }
       fence_mbarrier_init();
       {
@@ -718,9 +721,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         mbar_init(smem_u32(&bk.mma_ready[c]), 8);
         for (int q = 0; q < 4; ++q) mbar_arrive(smem_u32(&bk.mma_ready[c]));
       }
-      for (int a = 0; a < 2 * kNumA; ++a) mbar_init(smem_u32(&bk.a_empty[a]), 1);  // MMA commit
+      for (int a = 0; a < kNumA; ++a) mbar_init(smem_u32(&bk.a_empty[a]), 1);  // MMA commit
       for (int d = 0; d < 2 * kNumD; ++d) mbar_init(smem_u32(&bk.d_full[d]), 1);  // MMA commit
-      for (int q = 0; q < kNumSq; ++q) {
+      for (int q = 0; q < 2 * kNumSq; ++q) {
         mbar_init(smem_u32(&bk.sq_full[q]), 4);     // the four transform warps of the chunk
         mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the four accumulate warps of the chunk
       }
@@ -792,7 +795,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         mma_chunk_tf32x3(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t * 2 + (i & 1)]));
       else
         mma_chunk_exact(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t * 2 + (i & 1)]));
-      umma_commit_warp(smem_u32(&bk.a_empty[t * 2 + (k & 1)]));
+      umma_commit_warp(smem_u32(&bk.a_empty[t]));
     }
     if (!ok && lane == 0) fail(bk, P.err);
     // every MMA this warp issued completes before TMEM is released
@@ -819,36 +822,40 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                   kDrainLimitNs);
     }
   } else if (warp >= kFirstTWarp && warp < kFirstTWarp + kNumTWarps) {
-    // ---------------- transform warps: chunk k = 2L + h of x load L, into A
-    // buffer k % 3.  A parity wait for phase p of an mbarrier is only sound
-    // when the waiter already knows phase p - 1 complete: earlier, the wait
-    // cannot tell p - 2 (same parity) from p and returns at once.  Every wait
-    // below follows that rule: on full_x / chunk_done this half waited for
-    // the previous phase itself, and a_empty[k % 3][1 - h] carries exactly the
-    // chunks k - 3 of this half's chunks k.
-    const int h = (warp - kFirstTWarp) >> 2;
+    // ---------------- transform warps, three thirds of four (one warp per
+    // quadrant each): third tt takes the chunks k with k % 3 == tt, from half
+    // k % 2 of x load k / 2, into A buffer tt.  A parity wait for phase p of an
+    // mbarrier is only sound when the waiter already knows phase p - 1
+    // complete: earlier, the wait cannot tell p - 2 (same parity) from p and
+    // returns at once.  Every wait below follows that rule: with three x stages
+    // of two chunks, stage slot L % 3 always holds chunks of the same two
+    // thirds, so this third waits for every phase of the slots it uses;
+    // a_empty[tt] carries only this third's chunks; and chunk_done[s][h] (sum
+    // slot s, accumulate half h) only chunks of slots s that this third
+    // writes, whose phases it tracks bit by bit.
+    const int tt = (warp - kFirstTWarp) >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t xoff[8];  // byte offsets of the row's 16-byte pieces in a swizzled x tile
-#pragma unroll
-    for (int p = 0; p < 8; ++p) xoff[p] = (uint32_t)row * kRowBytes + ((uint32_t)(p ^ (row & 7)) << 4);
+    const uint32_t a_col = tmem + (uint32_t)tt * kACols;
+    uint32_t cd_par = 0;  // parity of the next phase of chunk_done[s][h]: bit (s / 3) * 2 + h
     bool ok = true;
-    for (int L = 0; L < n_loads; ++L) {
-      const int k = kChunksPerStage * L + h;
-      const int st = L % kXStages;
+    for (int k = tt; k < n_chunks; k += kNumA) {
+      const int L = k / kChunksPerStage, st = L % kXStages;
+      const int s = k % kNumSq, dh = (k / kChunksPerSlice) & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.full_x[st]),
                                              (uint32_t)(L / kXStages) & 1u, abort_flag,
                                              kWaitLimitNs));
       if (!ok) break;
-      const uint32_t xt = x_base + (uint32_t)st * kXBytes + (uint32_t)h * kXChunkBytes;
+      const uint32_t xt = x_base + (uint32_t)st * kXBytes + (uint32_t)(k % kChunksPerStage) * kXChunkBytes +
+                          (uint32_t)row * kRowBytes;
       uint32_t xw[32];
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const uint4 v = lds128(xt + xoff[p]);
+      for (int p = 0; p < 8; ++p) {  // the row's 16-byte pieces at their swizzled places
+        const uint4 v = lds128(xt + ((uint32_t)(p ^ (row & 7)) << 4));
         xw[4 * p] = v.x; xw[4 * p + 1] = v.y; xw[4 * p + 2] = v.z; xw[4 * p + 3] = v.w;
       }
-      // the row is in registers: this warp's half of the stage is released
+      // the row is in registers: this warp's part of the stage is released
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bk.empty_x[st]));
       const float tsq = sq_tree64_f32x2(xw);
@@ -875,31 +882,31 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
           xw[t] = bf16x2_sub(xw[t], lo[t]);  // x1, in place
         }
       }
-      // sq slot k % kNumSq is free once the accumulate warps have read chunk
-      // k - kNumSq; A buffer h once the MMAs of chunk k - 2 are done
+      // sum slot s is free once the accumulate half of chunk k - 6 has read
+      // it; A buffer tt once the MMAs of chunk k - 3 are done
       if (k >= kNumSq) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.chunk_done[k % kNumSq]),
-                                               (uint32_t)(k / kNumSq - 1) & 1u, abort_flag,
-                                               kWaitLimitNs));
+        const int hm = ((k - kNumSq) / kChunksPerSlice) & 1, bit = (s / kNumA) * 2 + hm;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.chunk_done[s * 2 + hm]),
+                                               (cd_par >> bit) & 1u, abort_flag, kWaitLimitNs));
+        cd_par ^= 1u << bit;
         if (!ok) break;
       }
-      sq_buf[(k % kNumSq) * kTileM + row] = tsq;
+      sq_buf[s * kTileM + row] = tsq;
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bk.sq_full[k % kNumSq]));
-      if (k >= kNumA) {  // chunk k - 3 (the other half's) is done with A buffer k % 3
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.a_empty[(k % kNumA) * 2 + (h ^ 1)]),
-                                               (uint32_t)((k - kNumA) / (2 * kNumA)) & 1u, abort_flag,
+      if (lane == 0) mbar_arrive(smem_u32(&bk.sq_full[s * 2 + dh]));
+      if (k >= kNumA) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.a_empty[tt]),
+                                               (uint32_t)(k / kNumA - 1) & 1u, abort_flag,
                                                kWaitLimitNs));
         if (!ok) break;
       }
       tc_fence_after();
-      const uint32_t a_col = tmem + (uint32_t)(k % kNumA) * kACols;
       tmem_st32(lanes | a_col, lo);
       tmem_st32(lanes | (a_col + 32), xw);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bk.mma_ready[k % kNumMma]));
+      if (lane == 0) mbar_arrive(smem_u32(&bk.mma_ready[tt]));
     }
     if (!ok) fail(bk, P.err);
   } else if (warp >= kFirstDWarp && warp < kFirstDWarp + kNumDWarps) {
@@ -947,9 +954,10 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const uint64_t keep = l2_policy_evict_last();  // the tail reads the partials next
-    // the parity of the next phase this half waits for on d_full[b][dh]
-    // (this half waits for every phase of its three barriers, in order)
-    uint32_t dpar = 0;
+    // the parity of the next phase this half waits for on d_full[b][dh] and
+    // sq_full[s][dh] (this half waits for every phase of those barriers, in
+    // order)
+    uint32_t dpar = 0, sqpar = 0;
     bool ok = true;
     for (int i = dh; ok && i < n; i += 2) {
       float2 acc[kMix / 2];
@@ -959,17 +967,18 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       for (int c = 0; c < kChunksPerSlice; ++c) {
         const int k = kChunksPerSlice * i + c, b = k % kNumD;
         // D of chunk k complete, and the chunk's sum of squares in its slot
-        // (slot k % 8 = 4 dh + c: only this half reads it)
+        const int sl = k % kNumSq;
         bool got = mbar_wait(smem_u32(&bk.d_full[b * 2 + dh]), (dpar >> b) & 1u, abort_flag,
                              kWaitLimitNs);
         dpar ^= 1u << b;
-        got = got && mbar_wait(smem_u32(&bk.sq_full[k % kNumSq]), (uint32_t)(k / kNumSq) & 1u,
-                               abort_flag, kWaitLimitNs);
+        got = got && mbar_wait(smem_u32(&bk.sq_full[sl * 2 + dh]), (sqpar >> sl) & 1u, abort_flag,
+                               kWaitLimitNs);
+        sqpar ^= 1u << sl;
         ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_col = tmem + kDCol0 + (uint32_t)b * kDCols<kTf32>;
-        const float tsq = sq_buf[(k % kNumSq) * kTileM + row];
+        const float tsq = sq_buf[sl * kTileM + row];
         if constexpr (kTf32) {
           uint32_t dv[kMix];
           tmem_ld16(lanes | d_col, dv);
@@ -978,7 +987,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
+            mbar_arrive(smem_u32(&bk.chunk_done[sl * 2 + dh]));
             mbar_arrive(smem_u32(&bk.mma_ready[b]));  // D buffer b free for chunk k + 3
           }
 #pragma unroll
@@ -987,33 +996,35 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                     __uint_as_float(dv[2 * j + 1])));
         } else {
           // D = [top | r1 | r2 | r3] (24 columns each); chunk dot = top + ((r1
-          // + r2) + r3).  Outputs 0..11 first, then 12..23 (two TMEM round
-          // trips keep the registers within the budget); the D buffer is
-          // handed back once the second round is in registers.
+          // + r2) + r3).  Outputs in kDRounds TMEM round trips of 24 / kDRounds
+          // (to stay within the registers); the D buffer is handed back once
+          // the last round is in registers.
+          constexpr int kCols = kMix / kDRounds;
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            uint32_t dv[4][12];
+          for (int r = 0; r < kDRounds; ++r) {
+            uint32_t dv[4][kCols];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-              tmem_ld8(lanes | (d_col + kMix * g + 12 * r), dv[g]);
-              tmem_ld4(lanes | (d_col + kMix * g + 12 * r + 8), dv[g] + 8);
+              tmem_ld8(lanes | (d_col + kMix * g + kCols * r), dv[g]);
+              if constexpr (kCols == 12) tmem_ld4(lanes | (d_col + kMix * g + kCols * r + 8), dv[g] + 8);
             }
             tmem_wait_ld();
-            if (r == 1) {
+            if (r == kDRounds - 1) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) {
-                mbar_arrive(smem_u32(&bk.chunk_done[k % kNumSq]));
+                mbar_arrive(smem_u32(&bk.chunk_done[sl * 2 + dh]));
                 mbar_arrive(smem_u32(&bk.mma_ready[b]));  // D buffer b free for chunk k + 3
               }
             }
 #pragma unroll
-            for (int j = 0; j < 6; ++j) {
+            for (int j = 0; j < kCols / 2; ++j) {
               const float2 top = make_float2(__uint_as_float(dv[0][2 * j]), __uint_as_float(dv[0][2 * j + 1]));
               const float2 u = make_float2(__uint_as_float(dv[1][2 * j]), __uint_as_float(dv[1][2 * j + 1]));
               const float2 v = make_float2(__uint_as_float(dv[2][2 * j]), __uint_as_float(dv[2][2 * j + 1]));
               const float2 w = make_float2(__uint_as_float(dv[3][2 * j]), __uint_as_float(dv[3][2 * j + 1]));
-              acc[6 * r + j] = __fadd2_rn(acc[6 * r + j], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
+              const int a = kCols / 2 * r + j;
+              acc[a] = __fadd2_rn(acc[a], __fadd2_rn(top, __fadd2_rn(__fadd2_rn(u, v), w)));
             }
           }
         }

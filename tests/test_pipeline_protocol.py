@@ -1,6 +1,6 @@
 """The tensor-core kernel's hand-off protocol, checked on the CPU.
 
-The kernel's roles (the x producer, two halves of four transform warps by
+The kernel's roles (the x producer, three thirds of four transform warps by
 chunk, three MMA issuers, two halves of four accumulate warps by unit, the
 W-slot refills) hand chunks to each other through mbarriers whose waits only test the
 parity of the phase they want.  Such a wait is sound only when the waiter
@@ -23,7 +23,7 @@ import random
 
 import pytest
 
-X_STAGES, N_A, N_D, N_SQ, SLOTS, N_MMA = 3, 3, 3, 8, 2, 3
+X_STAGES, N_A, N_D, N_SQ, SLOTS, N_MMA = 3, 3, 3, 6, 2, 3
 PLANTED = None  # a planted mistake for the tests that check the model has teeth
 
 
@@ -56,8 +56,9 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     for b in mma_ready:
         for _ in range(4):
             b.arrive()
-    a_empty = mk("a_empty", 1, 2 * N_A)  # [k % 3 * 2 + k % 2]: chunk k's MMAs done
-    sq_full, chunk_done = mk("sq_full", 4, N_SQ), mk("chunk_done", 4, N_SQ)
+    a_empty = mk("a_empty", 1, N_A)  # [k % 3]: chunk k's MMAs done
+    # [k % 6 * 2 + (k / 4) % 2]: sum slot of chunk k filled / read by its accumulate half
+    sq_full, chunk_done = mk("sq_full", 4, 2 * N_SQ), mk("chunk_done", 4, 2 * N_SQ)
     # d_full[b * 2 + h]: D buffer b holds a chunk of accumulate half h
     d_full, w_full = mk("d_full", 1, 2 * N_D), mk("w_full", 1, 4 * SLOTS)
     dconv = Bar(8, "dconv")
@@ -90,20 +91,25 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
             issue_load(L)
             yield None
 
-    def transform(h, q):
-        for L in range(nld):
-            k, st = 2 * L + h, L % X_STAGES
-            yield from wait(full_x[st], L // X_STAGES, f"T{h}{q} k{k} x")
+    def transform(tt, q):  # the chunks k with k % 3 == tt
+        cd_seen = {}  # phases of chunk_done[s][h] waited for so far
+        for k in range(tt, nck, N_A):
+            L, st = k // 2, (k // 2) % X_STAGES
+            s_, dh = k % N_SQ, (k // 4) % 2
+            yield from wait(full_x[st], L // X_STAGES, f"T{tt}{q} k{k} x")
             yield None
             x_read[L] += 1
             empty_x[st].arrive()
             if k >= N_SQ:
-                yield from wait(chunk_done[k % N_SQ], k // N_SQ - 1, f"T{h}{q} k{k} sq")
+                hm = ((k - N_SQ) // 4) % 2
+                key = s_ * 2 + hm
+                yield from wait(chunk_done[key], cd_seen.get(key, 0), f"T{tt}{q} k{k} sq")
+                cd_seen[key] = cd_seen.get(key, 0) + 1
                 check(sq_read[k - N_SQ] == 4, f"sq slot of chunk {k} over an unread one")
-            sq_full[k % N_SQ].arrive()
-            if k >= N_A:  # chunk k - 3 (the other half's) is done with A buffer k % 3
-                e = h if PLANTED == "own_half_a_empty" else h ^ 1
-                yield from wait(a_empty[(k % N_A) * 2 + e], (k - N_A) // (2 * N_A), f"T{h}{q} k{k} A")
+            sq_full[s_ * 2 + dh].arrive()
+            if k >= N_A:  # chunk k - 3 (this third's) is done with A buffer tt
+                a = (tt + 1) % N_A if PLANTED == "wrong_a_buffer" else tt
+                yield from wait(a_empty[a], k // N_A - 1, f"T{tt}{q} k{k} A")
                 check(k - N_A in mma_done, f"A buffer of chunk {k} rewritten before the MMAs of {k - N_A} were done")
             yield None
             mma_ready[k % N_MMA].arrive()
@@ -133,6 +139,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                     for c in range(4):
                         w_full[4 * j + c].arrive()
         seen = [0] * N_D  # phases of d_full[b * 2 + dh] waited for so far
+        sq_seen = [0] * N_SQ  # phases of sq_full[s * 2 + dh] waited for so far
         for i in range(dh, n, 2):
             for c in range(4):
                 k = 4 * i + c
@@ -140,12 +147,14 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                 dbar = b * 2 + dh if PLANTED != "d_full_by_buffer" else b * 2
                 yield from wait(d_full[dbar], seen[b], f"D{dh}{q} k{k}")
                 seen[b] += 1
-                yield from wait(sq_full[k % N_SQ], k // N_SQ, f"D{dh}{q} k{k} sq")
+                s_ = k % N_SQ
+                yield from wait(sq_full[s_ * 2 + dh], sq_seen[s_], f"D{dh}{q} k{k} sq")
+                sq_seen[s_] += 1
                 check(k in mma_done, f"D of chunk {k} read before its MMAs completed")
                 yield None
                 d_read[k] += 1
                 sq_read[k] += 1
-                chunk_done[k % N_SQ].arrive()
+                chunk_done[s_ * 2 + dh].arrive()
                 mma_ready[b].arrive()  # D buffer b free for chunk k + 3
             j = sl[i] - s_first
             if j + SLOTS < n_sl and (i == n - 1 or sl[i + 1] != sl[i]) and q == 0:
@@ -160,7 +169,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
         issue_load(L)
     roles = {"x": x_producer()}
     roles.update({f"I{g}": issuer(g) for g in range(N_MMA)})
-    roles.update({f"T{h}{q}": transform(h, q) for h in (0, 1) for q in range(4)})
+    roles.update({f"T{t}{q}": transform(t, q) for t in range(N_A) for q in range(4)})
     roles.update({f"D{h}{q}": accumulate(h, q) for h in (0, 1) for q in range(4)})
     state = {r: None for r in roles}
     done = set()
@@ -172,7 +181,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                 k, dbar = pipe.pop(0)  # the tensor pipe completes MMAs in issue order
                 mma_done.add(k)
                 d_full[dbar].arrive()
-                a_empty[(k % N_A) * 2 + k % 2].arrive()
+                a_empty[k % N_A].arrive()
             else:
                 st, _ = tma.pop(rnd.randrange(len(tma)))
                 full_x[st].arrive()
@@ -214,12 +223,11 @@ def test_protocol_sound_and_deadlock_free(M, K):
                 assert not errs, f"M={M} K={K} units {ub}+{n} seed {seed}: {errs[:3]}"
 
 
-@pytest.mark.parametrize("mistake", ["own_half_a_empty", "d_full_by_buffer"])
+@pytest.mark.parametrize("mistake", ["wrong_a_buffer", "d_full_by_buffer"])
 def test_model_catches_planted_mistakes(mistake):
-    """The checks have teeth: a transform half that waits for its own previous
-    chunk on A buffer k % 3 (instead of chunk k - 3, the other half's), or
-    accumulate halves that share one D barrier per buffer (each then sees only
-    some of its phases), are reported (an early return, a buffer rewritten too soon, or
+    """The checks have teeth: a transform third that waits on another third's
+    A barrier, or accumulate halves that share one D barrier per buffer (each
+    then sees only some of its phases), are reported (an early return, a buffer rewritten too soon, or
     the deadlock they lead to)."""
     global PLANTED
     PLANTED = mistake
