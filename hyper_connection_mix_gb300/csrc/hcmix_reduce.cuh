@@ -97,41 +97,48 @@ __device__ __forceinline__ void sinkhorn_rounds(float2 (&P)[kHc][kHc / 2], int i
   }
 }
 
-// The epilogue of one row, by one thread, from the row's totals (s_tot[j][r]:
-// j < 24 mix, j = 24 sum of squares): r = 1/sqrt(sq (1/K) + rms_eps); logit
-// j = mix_j r scale[g(j)] + base_j; pre = sigmoid, post = 2 sigmoid;
-// Sinkhorn on exp of the 16 comb logits, rows then columns, sums in index
-// order.  (hc_eps is added to every sum; the workloads use 0.)  Rows at or
+// The epilogue of one row, from the row's totals (s_tot[j][r]: j < 24 mix,
+// j = 24 sum of squares): r = 1/sqrt(sq (1/K) + rms_eps); logit j = mix_j r
+// scale[g(j)] + base_j; pre = sigmoid, post = 2 sigmoid; Sinkhorn on exp of
+// the 16 comb logits, rows then columns, sums in index order.  (hc_eps is
+// added to every sum; the workloads use 0.)  Four consecutive lanes share a
+// row: lane q computes pre q, post q and row q of exp(comb logits); lane 0
+// gathers the 16 values and runs the rounds (a chain of dependent steps that
+// does not split well).  Every lane of the warp calls this (the shuffles need
+// them all); `active` is the same for the four lanes of a row, and rows at or
 // past row_end are not written.
-__device__ __forceinline__ void epilogue_row(const float (&s_tot)[kPartStride][kReduceRows + 1],
-                                             int r, int row, int row_end, float inv_k,
-                                             const float* __restrict__ hc_scale,
-                                             const float* __restrict__ hc_base, int iters,
-                                             float rms_eps, float hc_eps,
-                                             float* __restrict__ pre, float* __restrict__ post,
-                                             float* __restrict__ comb) {
-  const float v = __fadd_rn(__fmul_rn(s_tot[kMix][r], inv_k), rms_eps);
+__device__ __forceinline__ void epilogue_row4(const float (&s_tot)[kPartStride][kReduceRows + 1],
+                                              int r, bool active, int row, int row_end, float inv_k,
+                                              const float* __restrict__ hc_scale,
+                                              const float* __restrict__ hc_base, int iters,
+                                              float rms_eps, float hc_eps,
+                                              float* __restrict__ pre, float* __restrict__ post,
+                                              float* __restrict__ comb) {
+  const int q = threadIdx.x & 3, base = (threadIdx.x & 31) & ~3;
+  const int rr_row = active ? r : 0;
+  const float v = __fadd_rn(__fmul_rn(s_tot[kMix][rr_row], inv_k), rms_eps);
   const float rr = rsqrt_fast(v);
-  float pp[2 * kHc];
-#pragma unroll
-  for (int e = 0; e < 2 * kHc; ++e) {
-    const float sc = e < kHc ? hc_scale[0] : hc_scale[1];
-    const float lg = __fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][r], rr), sc), hc_base[e]);
-    pp[e] = rcp_fast(__fadd_rn(1.0f, exp_fast(-lg)));  // (1 + e^-lg >= 1: no subnormal input)
-  }
-  auto comb_init = [&](float2 (&P)[kHc][kHc / 2]) {
-#pragma unroll
-    for (int i = 0; i < kHc; ++i)
-#pragma unroll
-      for (int h = 0; h < kHc / 2; ++h) {
-        const int e = 2 * kHc + kHc * i + 2 * h;
-        P[i][h] = make_float2(
-            exp_fast(__fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][r], rr), hc_scale[2]), hc_base[e])),
-            exp_fast(__fadd_rn(__fmul_rn(__fmul_rn(s_tot[e + 1][r], rr), hc_scale[2]), hc_base[e + 1])));
-      }
+  auto logit = [&](int e, float sc) {
+    return __fadd_rn(__fmul_rn(__fmul_rn(s_tot[e][rr_row], rr), sc), hc_base[e]);
   };
-  float2 P[kHc][kHc / 2];
-  comb_init(P);
+  const float p_pre = rcp_fast(__fadd_rn(1.0f, exp_fast(-logit(q, hc_scale[0]))));  // (>= 1: no subnormal)
+  const float p_post = rcp_fast(__fadd_rn(1.0f, exp_fast(-logit(kHc + q, hc_scale[1]))));
+  float c[kHc];  // row q of the comb matrix
+#pragma unroll
+  for (int jj = 0; jj < kHc; ++jj) c[jj] = exp_fast(logit(2 * kHc + kHc * q + jj, hc_scale[2]));
+  float2 P[kHc][kHc / 2];  // P[i][h] = (c[i][2h], c[i][2h+1]), gathered on lane q == 0
+#pragma unroll
+  for (int i = 0; i < kHc; ++i)
+#pragma unroll
+    for (int h = 0; h < kHc / 2; ++h)
+      P[i][h] = make_float2(__shfl_sync(0xffffffffu, c[2 * h], base + i),
+                            __shfl_sync(0xffffffffu, c[2 * h + 1], base + i));
+  const bool write = active && row < row_end;
+  if (write) {
+    pre[(int64_t)row * kHc + q] = p_pre;
+    post[(int64_t)row * kHc + q] = __fmul_rn(2.0f, p_post);
+  }
+  if (q != 0 || !active) return;
   if (hc_eps != 0.0f)
     sinkhorn_rounds<false, true>(P, iters, hc_eps);
   else
@@ -141,16 +148,16 @@ __device__ __forceinline__ void epilogue_row(const float (&s_tot)[kPartStride][k
   for (int i = 0; i < kHc; ++i) check += (P[i][0].x + P[i][0].y) + (P[i][1].x + P[i][1].y);
   if (!isfinite(check)) {
     // a sum fell below the normal range (or the inputs hold an infinity or
-    // NaN): again, dividing by the sums
-    comb_init(P);
+    // NaN): again from exp of the logits, dividing by the sums
+#pragma unroll
+    for (int i = 0; i < kHc; ++i)
+#pragma unroll
+      for (int h = 0; h < kHc / 2; ++h)
+        P[i][h] = make_float2(exp_fast(logit(2 * kHc + kHc * i + 2 * h, hc_scale[2])),
+                              exp_fast(logit(2 * kHc + kHc * i + 2 * h + 1, hc_scale[2])));
     sinkhorn_rounds<true, true>(P, iters, hc_eps);
   }
-  if (row >= row_end) return;
-#pragma unroll
-  for (int e = 0; e < kHc; ++e) {
-    pre[(int64_t)row * kHc + e] = pp[e];
-    post[(int64_t)row * kHc + e] = __fmul_rn(2.0f, pp[kHc + e]);
-  }
+  if (!write) return;
 #pragma unroll
   for (int i = 0; i < kHc; ++i)
 #pragma unroll
@@ -160,7 +167,9 @@ __device__ __forceinline__ void epilogue_row(const float (&s_tot)[kPartStride][k
     }
 }
 
-// The epilogue of the CTA's first nrows (<= 32) rows: one thread per row.
+// The epilogue of the CTA's first nrows (<= 32) rows: four lanes per row, the
+// first 4 * 32 threads (every lane of those warps takes part).
+constexpr int kEpilogueLanes = 4 * kReduceRows;
 __device__ __forceinline__ void epilogue_rows(const float (&s_tot)[kPartStride][kReduceRows + 1],
                                               int row0, int nrows, int row_end, float inv_k,
                                               const float* __restrict__ hc_scale,
@@ -169,9 +178,9 @@ __device__ __forceinline__ void epilogue_rows(const float (&s_tot)[kPartStride][
                                               float* __restrict__ pre, float* __restrict__ post,
                                               float* __restrict__ comb) {
   const int t = threadIdx.x;
-  if (t < nrows)
-    epilogue_row(s_tot, t, row0 + t, row_end, inv_k, hc_scale, hc_base, iters, rms_eps, hc_eps,
-                 pre, post, comb);
+  if (t < kEpilogueLanes)
+    epilogue_row4(s_tot, t >> 2, (t >> 2) < nrows, row0 + (t >> 2), row_end, inv_k, hc_scale,
+                  hc_base, iters, rms_eps, hc_eps, pre, post, comb);
 }
 
 __global__ void __launch_bounds__(kReduceThreads)
@@ -265,7 +274,7 @@ hcmix_reduce_small_kernel(const float* __restrict__ part, int n_slices, int Mpad
 // The epilogue alone from caller-provided mix[M, 24] and sq[M]: 32 rows per
 // CTA staged in shared memory in the reduce kernel's layout, then the same
 // one-thread-per-row epilogue.
-constexpr int kEpilogueThreads = kReduceRows;
+constexpr int kEpilogueThreads = kEpilogueLanes;
 
 __global__ void __launch_bounds__(kEpilogueThreads)
 hcmix_epilogue_kernel(const float* __restrict__ mix, const float* __restrict__ sq, int M,

@@ -150,6 +150,7 @@ struct Bookkeeping {
   uint64_t d_full[kNumD * 2];  // [b * 2 + (k / 4) % 2]: D buffer b holds chunk k, of accumulate half (k / 4) % 2
   uint64_t chunk_done[kNumSq * 2];  // [k % 6 * 2 + (k / 4) % 2]: the accumulate half has read it
   uint64_t w_full[kWBufs];
+  uint64_t w_stage;  // the fp32 W of the first two slices has landed in slot 1 (TMA)
   uint64_t drain[kNumMma];
   uint64_t tail_bar[6];
   uint32_t tmem_base;
@@ -161,6 +162,7 @@ struct Bookkeeping {
 static_assert(kDCol0 + kNumD * kDCols<false> <= kTmemCols &&
                   kDCol0 + kNumD * kDCols<true> <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Bookkeeping) <= 1024, "bookkeeping area");
+static_assert(3 + 3 + 6 + 12 < 31, "one barrier (pair) per lane of the initialising warp");
 static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of one unit");
 static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynamic shared memory");
 static_assert(Mode<false>::kBBytes % 1024 == 0 && Mode<true>::kBlockBytes % 1024 == 0,
@@ -667,7 +669,8 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   };
   // the fp32 W of slice index j (slot j % 2), converted by the `nthreads`
   // threads numbered `tid` from 0, a batch of each thread's W loads in flight
-  // at once
+  // at once.  (A CTA's first two slices come by TMA instead, staged in slot
+  // 1's buffers: see convert_staged.)
   auto convert_slice = [&](int j, int tid, int nthreads) {
     constexpr int kTasks = kMix * kChunksPerSlice;  // (output, chunk) pairs, 16 lanes each
     const int groups = nthreads / 16, sub = tid & 15;
@@ -698,6 +701,45 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
   };
 
+  // The first two slices' fp32 W, TMA-staged as [slice][24 rows][256] fp32 at
+  // the start of slot 1's buffers, converted by the 256 accumulate threads
+  // into slot j % 2 (thread `tid`; one batch: every load of a thread is made
+  // before any of its stores).  Slice 1 overwrites its own staging, so all
+  // threads first read it, then meet at a named barrier, then write (and the
+  // exact mode's zero rows of slot 1 come only then).
+  const uint32_t w_stage_base = wbuf(1, 0);
+  auto convert_staged = [&](int j, int tid) {
+    constexpr int kTasks = kMix * kChunksPerSlice;  // (output, chunk) pairs, 16 lanes each
+    constexpr int kThr = kNumDWarps * 32, kGroups = kThr / 16, kRounds = kTasks / kGroups;
+    static_assert(kTasks % kGroups == 0 && kRounds <= 8, "one batch of staged loads");
+    const int sub = tid & 15;
+    float4 wv[kRounds];
+#pragma unroll
+    for (int q = 0; q < kRounds; ++q) {
+      const int task = q * kGroups + (tid >> 4);
+      const uint4 v = lds128(w_stage_base + (uint32_t)j * (kMix * kSlice * 4) +
+                             (uint32_t)(task / kChunksPerSlice) * (kSlice * 4) +
+                             (uint32_t)(task % kChunksPerSlice) * (kChunk * 4) + (uint32_t)sub * 16);
+      wv[q] = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                          __uint_as_float(v.w));
+    }
+    if (j == 1) {
+      named_bar_sync(1, kThr);  // every thread has read slice 1's staging
+      if constexpr (!kTf32) {
+        constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
+        for (int idx = tid; idx < kChunksPerSlice * kUnits; idx += kThr) {
+          const int c = idx / kUnits, u = idx % kUnits;
+          sts128(wbuf(1, c) + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kRounds; ++q) {
+      const int task = q * kGroups + (tid >> 4);
+      convert_w4<kTf32>(wv[q], task / kChunksPerSlice, sub, wbuf(j, task % kChunksPerSlice), true);
+    }
+  };
+
   // ---- set-up.  Lane 0 of the x producer initialises the barriers (the x
   // ones first) and starts the first x loads (and, with prepacked limbs, the
   // W loads of the first two slices); warp 1 allocates TMEM; the transform
@@ -705,32 +747,25 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   // slice's fp32 W while the first x loads are in flight.
   if (warp == kXWarp) {
     if (lane == 0) {
+      mbar_init(smem_u32(&bk.w_stage), 1);
       for (int s = 0; s < kXStages; ++s) {
         mbar_init(smem_u32(&bk.full_x[s]), 1);
         mbar_init(smem_u32(&bk.empty_x[s]), kChunksPerStage * 4);  // the four transform warps of each chunk
       }
       fence_mbarrier_init();
+      if (P.w_src != nullptr) {  // the first two slices' fp32 W, ahead of the x loads
+        const int nw = min(kSlots, n_sl);
+        const uint64_t wpol = l2_policy_evict_last();
+        mbar_arrive_expect_tx(smem_u32(&bk.w_stage), (uint32_t)nw * (kMix * kSlice * 4));
+        for (int j = 0; j < nw; ++j)
+          tma_load_2d(w_stage_base + (uint32_t)j * (kMix * kSlice * 4), &tmap_w,
+                      (s_first + j) * kSlice, 0, smem_u32(&bk.w_stage), wpol);
+      }
       {
         const uint64_t pol = l2_policy_evict_first();
         for (int L = 0; L < kXStages && L < n_loads; ++L) issue_x_load(L, pol);
       }
-      // mma_ready[k % 3]: the four transform warps of chunk k and the four
-      // accumulate warps that have read chunk k - 3 (for the first three
-      // chunks, those four arrivals are made here)
-      for (int c = 0; c < kNumMma; ++c) {
-        mbar_init(smem_u32(&bk.mma_ready[c]), 8);
-        for (int q = 0; q < 4; ++q) mbar_arrive(smem_u32(&bk.mma_ready[c]));
-      }
-      for (int a = 0; a < kNumA; ++a) mbar_init(smem_u32(&bk.a_empty[a]), 1);  // MMA commit
-      for (int d = 0; d < 2 * kNumD; ++d) mbar_init(smem_u32(&bk.d_full[d]), 1);  // MMA commit
-      for (int q = 0; q < 2 * kNumSq; ++q) {
-        mbar_init(smem_u32(&bk.sq_full[q]), 4);     // the four transform warps of the chunk
-        mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the four accumulate warps of the chunk
-      }
       for (int w = 0; w < kWBufs; ++w) mbar_init(smem_u32(&bk.w_full[w]), 1);
-      for (int g = 0; g < kNumMma; ++g) mbar_init(smem_u32(&bk.drain[g]), 1);
-      bk.abort = 0;
-      bk.never = 0;
       fence_mbarrier_init();
       if constexpr (!kTf32) {
         if (P.w_src == nullptr) {
@@ -741,6 +776,28 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         }
       }
     }
+  } else if (warp == kMmaWarp0 + 2) {
+    // the other barriers, one or two per lane, while the producer's loads leave
+    if (lane < kNumMma) {
+      // mma_ready[k % 3]: the four transform warps of chunk k and the four
+      // accumulate warps that have read chunk k - 3 (for the first three
+      // chunks, those four arrivals are made here)
+      mbar_init(smem_u32(&bk.mma_ready[lane]), 8);
+      for (int q = 0; q < 4; ++q) mbar_arrive(smem_u32(&bk.mma_ready[lane]));
+      mbar_init(smem_u32(&bk.drain[lane]), 1);
+    } else if (lane < kNumMma + kNumA) {
+      mbar_init(smem_u32(&bk.a_empty[lane - kNumMma]), 1);  // MMA commit
+    } else if (lane < kNumMma + kNumA + 2 * kNumD) {
+      mbar_init(smem_u32(&bk.d_full[lane - kNumMma - kNumA]), 1);  // MMA commit
+    } else if (lane < kNumMma + kNumA + 2 * kNumD + 2 * kNumSq) {
+      const int q = lane - kNumMma - kNumA - 2 * kNumD;
+      mbar_init(smem_u32(&bk.sq_full[q]), 4);     // the four transform warps of the chunk
+      mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the four accumulate warps of the chunk
+    } else if (lane == 31) {
+      bk.abort = 0;
+      bk.never = 0;
+    }
+    fence_mbarrier_init();
   } else if (warp == kTmemWarp) {
     tmem_alloc(smem_u32(&bk.tmem_base), kTmemCols);
     tmem_relinquish();
@@ -748,10 +805,12 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // the zero rows of the exact-mode W buffers (the fp32 W itself is
     // converted by the accumulate warps after set-up, while the transform
     // warps already work on the first x loads)
+    // (slot 1 holds the staged fp32 W at first: its zero rows come later)
     const int tid = threadIdx.x - kFirstWorkWarp * 32, nthr = kThreads - kFirstWorkWarp * 32;
     if constexpr (!kTf32) {
       constexpr int kUnits = kLimbRowOffset * kRowBytes / 16;
-      for (int idx = tid; idx < kWBufs * kUnits; idx += nthr) {
+      const int nbufs = P.w_src != nullptr ? kChunksPerSlice : kWBufs;
+      for (int idx = tid; idx < nbufs * kUnits; idx += nthr) {
         const int w = idx / kUnits, u = idx % kUnits;
         sts128(w_base + (uint32_t)w * MD::kBBytes + (uint32_t)u * 16, make_uint4(0, 0, 0, 0));
       }
@@ -922,9 +981,12 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     if (dtid == 0 && P.tail != 0)  // (read before this CTA arrives; used after the teardown barrier)
       bk.gbar_base = ld_relaxed_gpu_u64(P.gbar) / kBarrierQuantum * kBarrierQuantum;
     if (P.w_src != nullptr) {
-      // the first two slices' W (the MMAs of each wait for its w_full)
+      // the first two slices' W, once their TMA has landed (the MMAs of
+      // each wait for its w_full)
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.w_stage), 0, abort_flag, kWaitLimitNs)))
+        fail(bk, P.err);
       for (int j = 0; j < kSlots && j < n_sl; ++j) {
-        convert_slice(j, dtid, kNumDWarps * 32);
+        convert_staged(j, dtid);
         fence_proxy_async_smem();
         named_bar_sync(1, kNumDWarps * 32);
         if (dtid == 0)
@@ -1123,6 +1185,21 @@ inline bool make_map_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor map: `inner` contiguous elements, `rows` rows `row_bytes`
+// apart; boxes of box_inner x box_rows, no swizzle (row-major in shared memory).
+inline bool make_map_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                            uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D view of a row-major bf16 matrix [rows, inner] as [inner / 64 chunks]
 // [rows][64]: one box is `box_chunks` consecutive 64-column chunks of
 // `box_rows` rows, stored in shared memory as box_chunks [box_rows x 128 B]
@@ -1210,8 +1287,8 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
     if (!tc::make_map_bf16_2d(&mw, packed, (uint64_t)K, tc::kLimbRows, (uint64_t)K * 2, kChunk,
                               tc::kLimbRows))
       return HCMIX_ERR_CUDA;
-  } else {
-    mw = mx;  // not used: W is converted inside the kernel
+  } else if (!tc::make_map_f32_2d(&mw, W, (uint64_t)K, kMix, (uint64_t)w_stride * 4, kSlice, kMix)) {
+    return HCMIX_ERR_CUDA;  // the fp32 W, TMA-staged for the first two slices of each CTA
   }
   tc::TcParams P = {};
   P.n_tiles = (int)((M + tc::kTileM - 1) / tc::kTileM);
