@@ -8,7 +8,7 @@
 // workload sizes (more only when K exceeds 152 slices), and the W operand of
 // those slices stays in shared memory for the whole range.
 //
-// One CTA = 20 warps with fixed roles, each role a stage of a pipeline over
+// One CTA = 24 warps with fixed roles, each role a stage of a pipeline over
 // the CTA's 64-column chunks (k = 0, 1, ... in unit order, four per unit).
 // Warp w runs on sub-partition w % 4 and may touch TMEM lanes 32 (w % 4)..:
 //   * warps 0..2, the MMA issuers: warp t issues the chunks with k % 3 == t,
@@ -17,34 +17,34 @@
 //     w2 | w3] against x0, so that
 //       D = [x0.w0 | x0.w1 + x1.w0 | x0.w2 + x1.w1 | x0.w3 + x1.w2]
 //     (the first 24 columns exact; x1.w3 ~ 2^-34 relative is dropped);
-//   * warp 3 (one lane), the x producer: TMA loads of two chunks of a tile
-//     (32 KB, 128-byte swizzle) into a 3-stage ring, the first ones during
-//     set-up.  It issues nothing else, so no other role's shared-memory
-//     accesses queue behind its copies;
-//   * warps 4..11, the transform warps, two halves of four (one per
-//     quadrant): half h takes the chunks with k % 2 == h.  Each thread reads
+//   * warp 3 (one lane), the x producer: it initialises the x barriers,
+//     TMA-loads the fp32 W of the CTA's first two slices (staged in slot 1's
+//     buffers) and then x, two chunks of a tile (32 KB, 128-byte swizzle) per
+//     load into a 3-stage ring.  It issues nothing else, so no other role's
+//     shared-memory accesses queue behind its copies;
+//   * warps 4..15, the transform warps, three thirds of four (one per
+//     quadrant): third t takes the chunks with k % 3 == t.  Each thread reads
 //     its row of the chunk from the x stage, sums its squares by the page's
 //     fixed tree, splits x into the limbs x0 (grid-aligned) and x1 = x - x0
-//     and stores both into TMEM A buffer k % 3 (x as fp32 in tf32x3 mode);
-//     the chunk's sum of squares goes to a shared-memory slot;
-//   * warps 12..19, the accumulate warps, two halves of four (one per
+//     and stores both into TMEM A buffer t (x as fp32 in tf32x3 mode); the
+//     chunk's sum of squares goes to a shared-memory slot;
+//   * warps 16..23, the accumulate warps, two halves of four (one per
 //     quadrant): half dh takes the units with i % 2 == dh, so that two
-//     units' reads are in flight at once.  They read D (two TMEM round trips
-//     of 4 x 12 columns), form the chunk dots fl32(top + ((r1 + r2) + r3)),
-//     add them into the slice totals (chunks in order, from zero), add the
+//     units' reads are in flight at once.  They read D (TMEM round trips of
+//     4 x 8 columns), form the chunk dots fl32(top + ((r1 + r2) + r3)), add
+//     them into the slice totals (chunks in order, from zero), add the
 //     chunk's sum of squares likewise, and store the 24 + 1 slice totals per
-//     row to the workspace partials at the end of the unit;
-//   * the W operand: every CTA converts the fp32 W of its first two slices
-//     into the exact bf16 limbs (or the tf32x3 big / small parts) in shared
-//     memory during set-up (no separate pack kernel); the accumulate warps
-//     refill a slot when the CTA covers more slices, or TMA-load limbs that
-//     hc_mix_pack_w wrote ahead of time.
+//     row to the workspace partials at the end of the unit.  Before that they
+//     convert the staged fp32 W into the exact bf16 limbs (or the tf32x3 big
+//     / small parts) in shared memory, and they refill a slot when the CTA
+//     covers more slices (or TMA-load limbs that hc_mix_pack_w wrote ahead);
+//   * warp 2 also initialises the hand-off barriers during set-up.
 // The A and D rings are three deep, so that neither hand-off loop (A buffer:
 // written, MMAs issued and completed, rewritten; D buffer: MMAs completed,
 // read, next MMAs issued) spans fewer than three chunks.  Every mbarrier wait
 // is by a waiter that has seen the barrier's previous phase, as a parity wait
-// needs: A buffer k % 3 is freed on a_empty[k % 3][k % 2], which only the
-// other transform half (the writer of chunk k + 3) waits on.
+// needs: each A buffer, D buffer (per accumulate half), sum slot (per half)
+// and x stage slot has fixed waiters that see every phase.
 //
 // Tail (same kernel): once every CTA has stored its partials (a grid-wide
 // barrier; the launch is cooperative, so every CTA is resident), CTA b adds
