@@ -741,12 +741,16 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   };
 
   // ---- set-up.  Lane 0 of the x producer initialises the barriers (the x
-  // ones first) and starts the first x loads (and, with prepacked limbs, the
-  // W loads of the first two slices); warp 1 allocates TMEM; the transform
-  // and accumulate warps zero the W buffers' zero rows and convert the first
-  // slice's fp32 W while the first x loads are in flight.
+  // ones first) and starts the W staging and the first x load (and, with
+  // prepacked limbs, the W loads of the first two slices); warp 1 allocates
+  // TMEM; the transform and accumulate warps zero the W buffers' zero rows.
+  // The other first x loads leave once set-up is done: with every CTA's first
+  // loads in flight at once, each load lands only when nearly all of them
+  // have, so fewer at first bring the first chunk in sooner.
   if (warp == kXWarp) {
     if (lane == 0) {
+      prefetch_tensormap(&tmap_x);
+      prefetch_tensormap(&tmap_w);  // the fp32 W, or the packed limbs
       mbar_init(smem_u32(&bk.w_stage), 1);
       for (int s = 0; s < kXStages; ++s) {
         mbar_init(smem_u32(&bk.full_x[s]), 1);
@@ -763,13 +767,12 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       }
       {
         const uint64_t pol = l2_policy_evict_first();
-        for (int L = 0; L < kXStages && L < n_loads; ++L) issue_x_load(L, pol);
+        if (n_loads > 0) issue_x_load(0, pol);
       }
       for (int w = 0; w < kWBufs; ++w) mbar_init(smem_u32(&bk.w_full[w]), 1);
       fence_mbarrier_init();
       if constexpr (!kTf32) {
         if (P.w_src == nullptr) {
-          prefetch_tensormap(&tmap_w);
           const uint64_t wpol = l2_policy_evict_last();
           for (int j = 0; j < kSlots && j < n_sl; ++j)
             for (int c = 0; c < kChunksPerSlice; ++c) issue_w_load(j, c, s_first + j, wpol);
@@ -861,14 +864,15 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     umma_commit_warp(smem_u32(&bk.drain[t]));
     mbar_wait(smem_u32(&bk.drain[t]), 0, never, kDrainLimitNs);
   } else if (warp == kXWarp) {
-    // ---------------- x producer: the loads after the first kXStages, each
-    // once the transform warps have read the stage's previous load
+    // ---------------- x producer: the loads after the first, each (after the
+    // first kXStages) once the transform warps have read the stage's previous
+    // load
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      int L = kXStages;
+      int L = 1;
       for (; L < n_loads; ++L) {
         const int st = L % kXStages;
-        if (!mbar_wait(smem_u32(&bk.empty_x[st]), (uint32_t)(L / kXStages - 1) & 1u, abort_flag,
+        if (L >= kXStages && !mbar_wait(smem_u32(&bk.empty_x[st]), (uint32_t)(L / kXStages - 1) & 1u, abort_flag,
                        kWaitLimitNs)) {
           fail(bk, P.err);
           break;

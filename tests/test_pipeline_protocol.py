@@ -85,9 +85,10 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
         check(L < X_STAGES or x_read[L - X_STAGES] == 8, f"x load {L} over an unread stage")
         tma.append((L % X_STAGES, L))
 
-    def x_producer():
-        for L in range(X_STAGES, nld):
-            yield from wait(empty_x[L % X_STAGES], L // X_STAGES - 1, f"x L{L}")
+    def x_producer():  # the loads after the first (set-up issues load 0)
+        for L in range(1, nld):
+            if L >= X_STAGES:
+                yield from wait(empty_x[L % X_STAGES], L // X_STAGES - 1, f"x L{L}")
             issue_load(L)
             yield None
 
@@ -165,8 +166,8 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     if packed:
         for c in range(4 * min(SLOTS, n_sl)):
             w_full[c].arrive()  # set-up: TMA loads of the first two slices' limbs
-    for L in range(min(X_STAGES, nld)):  # set-up: the first x loads
-        issue_load(L)
+    if nld:  # set-up: the first x load
+        issue_load(0)
     roles = {"x": x_producer()}
     roles.update({f"I{g}": issuer(g) for g in range(N_MMA)})
     roles.update({f"T{t}{q}": transform(t, q) for t in range(N_A) for q in range(4)})
