@@ -152,7 +152,7 @@ struct Bookkeeping {
   uint64_t w_full[kWBufs];
   uint64_t w_stage;  // the fp32 W of the first two slices has landed in slot 1 (TMA)
   uint64_t drain[kNumMma];
-  uint64_t tail_bar[6];
+  uint64_t tail_bar[6];  // the tail's copy slots (kTailSlots)
   uint32_t tmem_base;
   unsigned long long gbar_base;  // the grid barrier's counter before this CTA arrived, rounded down
   int abort;
@@ -162,7 +162,7 @@ struct Bookkeeping {
 static_assert(kDCol0 + kNumD * kDCols<false> <= kTmemCols &&
                   kDCol0 + kNumD * kDCols<true> <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Bookkeeping) <= 1024, "bookkeeping area");
-static_assert(3 + 3 + 6 + 12 < 31, "one barrier (pair) per lane of the initialising warp");
+static_assert(3 + 3 + 6 + 12 + 6 < 31, "one barrier (pair) per lane of the initialising warp");
 static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of one unit");
 static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynamic shared memory");
 static_assert(Mode<false>::kBBytes % 1024 == 0 && Mode<true>::kBlockBytes % 1024 == 0,
@@ -186,7 +186,8 @@ struct TcParams {
   int n_slices;    // K / 256
   int M, Mpad;
   int64_t n_units;
-  float* part;     // workspace partials [n_slices][25][Mpad]
+  float* part;     // workspace partials, groups of 1 << g_shift rows (see part_index)
+  int g_shift;     // log2 of the rows per partial group: 3, or fewer for M < 5
   uint32_t* err;   // device error word
   unsigned long long* gbar;  // the grid barrier's counter (workspace header)
   const float* w_src;  // fp32 W, converted in-kernel; null: limbs come by TMA
@@ -514,19 +515,27 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* counter, unsign
 
 // ---------------------------------------------------------------- partials
 
-// The tensor-core path stores the slice totals of 8-row groups ("octs")
-// contiguously, so that the rows a CTA reduces arrive in a few bulk copies:
-// value j (24 mix values, then the sum of squares) of slice s for row r sits at
-//   part[((r / 8 * n_slices + s) * 25 + j) * 8 + r % 8].
-// A warp's 32 rows of one (s, j) are four full 32-byte sectors.
-__device__ __forceinline__ int64_t part_index(int row, int s, int j, int n_slices) {
-  return ((int64_t)(row >> 3) * n_slices + s) * (kPartStride * 8) + j * 8 + (row & 7);
+// The tensor-core path stores the slice totals of R-row groups contiguously
+// (R = 8, or the power of two at or above M when M < 5), so that the rows a
+// CTA reduces arrive in a few bulk copies: value j (24 mix values, then the
+// sum of squares) of slice s for row r sits at
+//   part[((r / R * n_slices + s) * 25 + j) * R + r % R].
+// With R = 8 a warp's 32 rows of one (s, j) are four full 32-byte sectors;
+// the narrower groups keep a decode call's reduce from reading the partials
+// of rows that do not exist.
+__device__ __forceinline__ int64_t part_index(int row, int s, int j, int n_slices, int gs) {
+  return ((((int64_t)(row >> gs) * n_slices + s) * kPartStride + j) << gs) +
+         (row & ((1 << gs) - 1));
+}
+__host__ __device__ inline int part_group_shift(int64_t M) {
+  return M >= 5 ? 3 : M >= 3 ? 2 : M == 2 ? 1 : 0;
 }
 
 constexpr int kTailSlices = 40;                                      // slices per bulk copy
 constexpr uint32_t kTailSlotBytes = kTailSlices * kPartStride * 8 * 4;  // 32000
 constexpr int kTailSlotsPerHalf = 3;
 constexpr int kTailSlots = 2 * kTailSlotsPerHalf;                    // three per half of the CTA
+static_assert(sizeof(Bookkeeping::tail_bar) == kTailSlots * sizeof(uint64_t), "tail slots");
 constexpr size_t kTailTotOff = (size_t)kTailSlots * kTailSlotBytes;
 constexpr size_t kTailParOff = kTailTotOff + (size_t)kPartStride * (kReduceRows + 1) * 4;
 constexpr size_t kTailBytes = (kTailParOff + 32 * 4 + 15) / 16 * 16;  // shared memory the tail uses
@@ -534,81 +543,125 @@ constexpr int kTailThreads = 512;
 // the tail reuses the x / W buffers; the bookkeeping (its barriers) lies past them
 static_assert(kTailBytes <= kBkOff<false> && kTailBytes <= kBkOff<true>, "tail shared memory");
 
-// The tail of a call for CTA b of G: the octs [b n / G, (b + 1) n / G) of the
-// n = ceil(M / 8) octs.  Each half of the CTA (256 threads) takes every other
-// oct; its thread t < 200 owns value j = t / 8 of row t % 8 and adds that
-// value's slice totals in slice order from zero, reading them from bulk
-// copies of up to 40 slices (three slots per half, all in flight from the
-// start, each refilled once added up).  Every 4 octs (32 rows) the CTA writes
-// mix / sq (when asked for) and, with P.tail == 2, runs the epilogue on those
-// rows, one thread per row.  `tb`: kTailBytes of shared memory (16-byte
-// aligned); `tbar`: kTailSlots mbarriers;
-// `never`: a flag that stays 0 (the waits here are bounded by time only).
-__device__ __forceinline__ void tc_tail(const TcParams& P, uint8_t* tb, uint64_t* tbar,
-                                        const volatile int* never, int64_t b, int64_t G) {
+// The tail of a call for CTA b of G: the row groups [b n / G, (b + 1) n / G)
+// of the n = ceil(M / R) groups of R = 1 << P.g_shift rows.  Each half of the
+// CTA (256 threads) takes every other group; its thread t < 25 R owns value
+// j = t / R of row t % R and adds that value's slice totals in slice order
+// from zero, reading them from bulk copies of up to 40 R' slices, R' = 8 / R
+// (three slots per half, all in flight from the start, each refilled once
+// added up).  Every 4 groups (at most 32 rows) the CTA writes mix / sq (when
+// asked for) and, with P.tail == 2, runs the epilogue on those rows, four
+// lanes per row.  `tb`: kTailBytes of shared memory (16-byte aligned);
+// `tbar`: kTailSlots mbarriers, initialised with count 1.  Its three steps:
+//   tail_params   (threads 0..26) hc_scale and hc_base into shared memory;
+//   tail_start    (one thread, after the partials are visible) the first
+//                 copies of both halves;
+//   tc_tail       (every thread, after a CTA barrier) the rest;
+// all three from the same TailPlan, which every thread can make beforehand.
+struct TailPlan {
+  int gs, R, n_grp, o0, o1, ns, per_piece, n_pieces;
+  __device__ TailPlan(const TcParams& P, int64_t b, int64_t G) {
+    gs = P.g_shift;
+    R = 1 << gs;
+    n_grp = (P.M + R - 1) >> gs;
+    o0 = (int)(b * n_grp / G);
+    o1 = (int)((b + 1) * n_grp / G);
+    ns = P.n_slices;
+    per_piece = kTailSlices << (3 - gs);  // a slot holds 40 slices of 8 rows
+    n_pieces = (ns + per_piece - 1) / per_piece;
+  }
+  __device__ int groups_of_half(int h) const {  // groups o0 + h, o0 + h + 2, ...
+    return h < 2 && o1 - o0 > h ? (o1 - o0 - h + 1) / 2 : 0;
+  }
+  // item i of half h (group, piece) into its slot i % 3
+  __device__ void issue(const TcParams& P, uint8_t* tb, uint64_t* tbar, int h, int i) const {
+    using namespace sm100;
+    const int grp = o0 + h + 2 * (i / n_pieces), s0 = (i % n_pieces) * per_piece;
+    // (rounded up to whole 16-byte units: the extra bytes lie inside the
+    // workspace, which holds 128 rows per tile, and are never read)
+    const uint32_t bytes =
+        ((uint32_t)min(per_piece, ns - s0) * (kPartStride * 4 << gs) + 15) & ~15u;
+    const int slot = kTailSlotsPerHalf * h + i % kTailSlotsPerHalf;
+    const uint32_t bar = smem_u32(&tbar[slot]);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(smem_u32(tb) + (uint32_t)slot * kTailSlotBytes,
+              P.part + ((((int64_t)grp * ns + s0) * kPartStride) << gs), bytes, bar,
+              l2_policy_evict_first());
+  }
+};
+static_assert(kTailSlices * kPartStride * 8 * 4 == (int)kTailSlotBytes, "a slot: 40 slices of 8 rows");
+
+__device__ __forceinline__ void tail_params(const TcParams& P, uint8_t* tb) {
+  float* s_par = reinterpret_cast<float*>(tb + kTailParOff);  // hc_scale[3], hc_base[24]
+  const int tid = threadIdx.x;
+  if (P.tail == 2 && tid < 3 + kMix) s_par[tid] = tid < 3 ? P.hc_scale[tid] : P.hc_base[tid - 3];
+}
+
+__device__ __forceinline__ void tail_start(const TcParams& P, const TailPlan& T, uint8_t* tb,
+                                           uint64_t* tbar) {
+  // the partials were written by other CTAs through the generic proxy, and
+  // the slots were last used through it
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  sm100::fence_proxy_async_smem();
+  for (int h = 0; h < 2; ++h) {
+    const int n_items = T.groups_of_half(h) * T.n_pieces;
+    for (int i = 0; i < kTailSlotsPerHalf && i < n_items; ++i) T.issue(P, tb, tbar, h, i);
+  }
+}
+
+__device__ __forceinline__ void tc_tail(const TcParams& P, const TailPlan& T, uint8_t* tb,
+                                        uint64_t* tbar, const volatile int* never) {
   using namespace sm100;
   const int tid = threadIdx.x;
-  const int n_octs = (P.M + 7) / 8;
-  const int o0 = (int)(b * n_octs / G), o1 = (int)((b + 1) * n_octs / G);
+  const int gs = T.gs;
   auto& s_tot = *reinterpret_cast<float (*)[kPartStride][kReduceRows + 1]>(tb + kTailTotOff);
-  float* s_par = reinterpret_cast<float*>(tb + kTailParOff);  // hc_scale[3], hc_base[24]
-  if (P.tail == 2 && tid < 3 + kMix) s_par[tid] = tid < 3 ? P.hc_scale[tid] : P.hc_base[tid - 3];
-  const int ns = P.n_slices;
-  const int n_pieces = (ns + kTailSlices - 1) / kTailSlices;
-  // threads past the two halves (the kernel has a warp more) only join the CTA barriers
+  const float* s_par = reinterpret_cast<const float*>(tb + kTailParOff);
+  // threads past the two halves (the kernel has more warps) only join the CTA barriers
   const int h = min(tid >> 8, 2), t = tid & 255;
-  const int my_octs = h < 2 && o1 - o0 > h ? (o1 - o0 - h + 1) / 2 : 0;  // octs o0 + h, o0 + h + 2, ...
-  const int n_items = my_octs * n_pieces;                       // item = (oct, piece)
-  const uint32_t slot0 = smem_u32(tb) + (uint32_t)(kTailSlotsPerHalf * min(h, 1)) * kTailSlotBytes;
-  const uint32_t bar0 = smem_u32(&tbar[kTailSlotsPerHalf * min(h, 1)]);
-  auto issue = [&](int i) {  // item i of this half into its slot i % 3
-    const int oct = o0 + h + 2 * (i / n_pieces), s0 = (i % n_pieces) * kTailSlices;
-    const uint32_t bytes = (uint32_t)min(kTailSlices, ns - s0) * (kPartStride * 8 * 4);
-    const uint32_t bar = bar0 + (uint32_t)(i % kTailSlotsPerHalf) * 8;
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(slot0 + (uint32_t)(i % kTailSlotsPerHalf) * kTailSlotBytes,
-              P.part + ((int64_t)oct * ns + s0) * (kPartStride * 8), bytes, bar,
-              l2_policy_evict_first());
-  };
-  if (tid == 0) {
-    for (int q = 0; q < kTailSlots; ++q) mbar_init(smem_u32(&tbar[q]), 1);
-    fence_mbarrier_init();
-  }
-  cta_barrier();
-  if (t == 0 && h < 2) {
-    // the partials were written by other CTAs through the generic proxy
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    for (int i = 0; i < kTailSlotsPerHalf && i < n_items; ++i) issue(i);
-  }
-  const int j = t >> 3, r8 = t & 7;
-  const int n_groups = (o1 - o0 + 3) / 4;
+  const int my_grps = T.groups_of_half(h);
+  const int n_items = my_grps * T.n_pieces;  // item = (group, piece)
+  const int j = t >> gs, r8 = t & (T.R - 1);
+  const bool adder = h < 2 && t < (kPartStride << gs);
+  const int vstride = kPartStride << gs;  // one slice
+  const int n_groups = (T.o1 - T.o0 + 3) / 4;
   int i = 0;
   for (int g = 0; g < n_groups; ++g) {
     for (int q = 0; q < 2; ++q) {
-      const int m = 2 * g + q;  // this half's m-th oct
-      if (m >= my_octs) continue;
+      const int m = 2 * g + q;  // this half's m-th group
+      if (m >= my_grps) continue;
       float tot = 0.0f;
-      for (int p = 0; p < n_pieces; ++p, ++i) {
-        if (!mbar_wait(bar0 + (uint32_t)(i % kTailSlotsPerHalf) * 8,
-                       (uint32_t)(i / kTailSlotsPerHalf) & 1u, never, kWaitLimitNs))
+      for (int p = 0; p < T.n_pieces; ++p, ++i) {
+        const int slot = kTailSlotsPerHalf * h + i % kTailSlotsPerHalf;
+        if (!mbar_wait(smem_u32(&tbar[slot]), (uint32_t)(i / kTailSlotsPerHalf) & 1u, never,
+                       kWaitLimitNs))
           record_device_error(P.err, kDevWaitTimeout);
-        if (t < kPartStride * 8) {
-          const float* v = reinterpret_cast<const float*>(
-              tb + (size_t)(kTailSlotsPerHalf * h + i % kTailSlotsPerHalf) * kTailSlotBytes);
-          const int cnt = min(kTailSlices, ns - p * kTailSlices);
-#pragma unroll 8
-          for (int s = 0; s < cnt; ++s) tot = __fadd_rn(tot, v[(s * kPartStride + j) * 8 + r8]);
+        if (adder) {
+          // slice s of value j of row r8 at ((s 25 + j) R + r8); eight loads
+          // at a time, then their adds in slice order (plain loads: the
+          // compiler issues them together)
+          const float* v0 = reinterpret_cast<const float*>(tb + (size_t)slot * kTailSlotBytes) +
+                            (j << gs) + r8;
+          const int cnt = min(T.per_piece, T.ns - p * T.per_piece);
+          int s = 0;
+          for (; s + 8 <= cnt; s += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = v0[(s + u) * vstride];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) tot = __fadd_rn(tot, v[u]);
+          }
+          for (; s < cnt; ++s) tot = __fadd_rn(tot, v0[s * vstride]);
         }
         named_bar_sync(1 + h, 256);  // the half has read the slot
-        if (t == 0 && i + kTailSlotsPerHalf < n_items) issue(i + kTailSlotsPerHalf);
+        if (t == 0 && i + kTailSlotsPerHalf < n_items) T.issue(P, tb, tbar, h, i + kTailSlotsPerHalf);
       }
-      if (t < kPartStride * 8) s_tot[j][(h + 2 * q) * 8 + r8] = tot;
+      if (adder) s_tot[j][((h + 2 * q) << gs) + r8] = tot;
     }
     cta_barrier();
-    const int r0 = (o0 + 4 * g) * 8;
-    const int nr = min(min(32, (o1 - o0 - 4 * g) * 8), P.M - r0);
+    const int r0 = (T.o0 + 4 * g) << gs;
+    const int nr = min(min(4 << gs, (T.o1 - T.o0 - 4 * g) << gs), P.M - r0);
     if (P.mix_out != nullptr)
-      for (int e = tid; e < nr * kMix; e += kTailThreads)
+      for (int e = tid; e < nr * kMix; e += blockDim.x)
         P.mix_out[(int64_t)(r0 + e / kMix) * kMix + e % kMix] = s_tot[e % kMix][e / kMix];
     if (P.sq_out != nullptr && tid < nr) P.sq_out[r0 + tid] = s_tot[kMix][tid];
     if (P.tail == 2)
@@ -796,6 +849,8 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       const int q = lane - kNumMma - kNumA - 2 * kNumD;
       mbar_init(smem_u32(&bk.sq_full[q]), 4);     // the four transform warps of the chunk
       mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the four accumulate warps of the chunk
+    } else if (lane < kNumMma + kNumA + 2 * kNumD + 2 * kNumSq + kTailSlots) {
+      mbar_init(smem_u32(&bk.tail_bar[lane - kNumMma - kNumA - 2 * kNumD - 2 * kNumSq]), 1);
     } else if (lane == 31) {
       bk.abort = 0;
       bk.never = 0;
@@ -1097,13 +1152,17 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         sqs = __fadd_rn(sqs, tsq);
       }
       if (!ok) break;
-      float* p = P.part + part_index(unit_tile(i) * kTileM + row, unit_slice(i), 0, P.n_slices);
+      const int grow = unit_tile(i) * kTileM + row;
+      if (grow < P.M) {  // (the rows past M of the last tile are zeros: not stored)
+        const int gs = P.g_shift;
+        float* p = P.part + part_index(grow, unit_slice(i), 0, P.n_slices, gs);
 #pragma unroll
-      for (int j = 0; j < kMix / 2; ++j) {
-        stg_f32_hint(p + 8 * (2 * j), acc[j].x, keep);
-        stg_f32_hint(p + 8 * (2 * j + 1), acc[j].y, keep);
+        for (int j = 0; j < kMix / 2; ++j) {
+          stg_f32_hint(p + ((2 * j) << gs), acc[j].x, keep);
+          stg_f32_hint(p + ((2 * j + 1) << gs), acc[j].y, keep);
+        }
+        stg_f32_hint(p + (kMix << gs), sqs, keep);
       }
-      stg_f32_hint(p + 8 * kMix, sqs, keep);
       // the last unit of slice j done: slice j + 2 (if any) may take its slot
       const int j = unit_slice(i) - s_first;
       if (j + kSlots < n_sl && (i == n - 1 || unit_slice(i + 1) != unit_slice(i)))
@@ -1131,12 +1190,18 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
   // ---- tail: once every CTA's partials are stored (grid barrier) this CTA
   // adds the slices of its rows in slice order and runs the epilogue; the x
-  // and W buffers are idle now and hold the tail's copies
-  if (threadIdx.x == 0 &&
-      !grid_barrier(P.gbar, bk.gbar_base, b, G, kWaitLimitNs))
-    record_device_error(P.err, kDevWaitTimeout);
+  // and W buffers are idle now and hold the tail's copies (the epilogue's
+  // parameters are loaded while the barrier waits, the first copies leave as
+  // soon as it opens)
+  tail_params(P, smem);
+  const TailPlan T(P, b, G);
+  if (threadIdx.x == 0) {
+    if (!grid_barrier(P.gbar, bk.gbar_base, b, G, kWaitLimitNs))
+      record_device_error(P.err, kDevWaitTimeout);
+    tail_start(P, T, smem, bk.tail_bar);
+  }
   cta_barrier();
-  tc_tail(P, smem, bk.tail_bar, never, b, G);
+  tc_tail(P, T, smem, bk.tail_bar, never);
 }
 
 // The tail alone (HCMIX_PATH_TC_STAGED): the same reduce and epilogue as the
@@ -1147,8 +1212,16 @@ __global__ void __launch_bounds__(kTailThreads, 1) hcmix_tc_tail_kernel(const __
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
   uint64_t* tbar = reinterpret_cast<uint64_t*>(tb + kTailBytes);
   __shared__ int never;
-  if (threadIdx.x == 0) never = 0;  // ordered before any wait by the barrier inside the tail
-  tc_tail(P, tb, tbar, &never, blockIdx.x, gridDim.x);
+  tail_params(P, tb);
+  const TailPlan T(P, blockIdx.x, gridDim.x);
+  if (threadIdx.x == 0) {
+    never = 0;
+    for (int q = 0; q < kTailSlots; ++q) sm100::mbar_init(sm100::smem_u32(&tbar[q]), 1);
+    sm100::fence_mbarrier_init();
+    tail_start(P, T, tb, tbar);
+  }
+  __syncthreads();
+  tc_tail(P, T, tb, tbar, &never);
 }
 constexpr size_t kTailKernelSmem = kTailBytes + kTailSlots * 8 + 128;
 
@@ -1298,6 +1371,7 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
   P.n_tiles = (int)((M + tc::kTileM - 1) / tc::kTileM);
   P.n_slices = (int)(K / kSlice);
   P.M = (int)M;
+  P.g_shift = tc::part_group_shift(M);
   P.Mpad = Mpad;
   P.n_units = (int64_t)P.n_tiles * P.n_slices;
   P.part = part;

@@ -80,8 +80,8 @@ def check_all(x, W, sc, bs, path, what, **kw):
     return r
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 7, 8])
-@pytest.mark.parametrize("K", [256, 512, 1024])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])
+@pytest.mark.parametrize("K", [256, 512, 768, 1024])
 def test_tiny(path, M, K):
     x = hi.make_x(M, K=K)
     check_all(x, hi.make_w(K=K), hi.make_scale(), hi.make_base(), path, f"M={M} K={K}")
