@@ -185,7 +185,8 @@ struct TcParams {
   int n_tiles;     // 128-row tiles
   int n_slices;    // K / 256
   int M, Mpad;
-  int64_t n_units;
+  int64_t n_units;  // < 2^31 (the host checks)
+  int units_q, units_r;  // n_units = units_q * grid + units_r
   float* part;     // workspace partials, groups of 1 << g_shift rows (see part_index)
   int g_shift;     // log2 of the rows per partial group: 3, or fewer for M < 5
   uint32_t* err;   // device error word
@@ -687,12 +688,17 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int64_t G = gridDim.x, b = blockIdx.x;
-  const int64_t u_begin = b * P.n_units / G;
-  const int n = (int)((b + 1) * P.n_units / G - u_begin);  // units of this CTA, >= 1
+  // units [b n_units / G, (b + 1) n_units / G), in 32-bit arithmetic:
+  // floor(b (q G + r) / G) = b q + floor(b r / G), with b r < G^2
+  const uint32_t ub = (uint32_t)b, ug = (uint32_t)G;
+  const uint32_t u_begin = ub * (uint32_t)P.units_q + ub * (uint32_t)P.units_r / ug;
+  const uint32_t u_end = (ub + 1) * (uint32_t)P.units_q + (ub + 1) * (uint32_t)P.units_r / ug;
+  const int n = (int)(u_end - u_begin);  // units of this CTA, >= 1
   const int n_chunks = kChunksPerSlice * n;
   const int n_loads = n_chunks / kChunksPerStage;
-  const int s_first = (int)(u_begin / P.n_tiles);
-  const int n_sl = (int)((u_begin + n - 1) / P.n_tiles) - s_first + 1;  // slices of this CTA
+  const uint32_t n_tiles = (uint32_t)P.n_tiles;
+  const int s_first = (int)(u_begin / n_tiles);
+  const int n_sl = (int)((u_end - 1) / n_tiles) - s_first + 1;  // slices of this CTA
 
   const uint32_t x_base = smem_u32(smem + kXOff<kTf32>);
   const uint32_t w_base = smem_u32(smem + kWOff<kTf32>);
@@ -701,7 +707,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   };
   // unit i of this CTA: tile (u % n_tiles) of slice (u / n_tiles), u = u_begin + i
   // (32-bit arithmetic from the CTA's first unit: i < n, and n_tiles fits)
-  const int tile0 = (int)(u_begin % P.n_tiles);
+  const int tile0 = (int)(u_begin % n_tiles);
   auto unit_tile = [&](int i) { return (tile0 + i) % P.n_tiles; };
   auto unit_slice = [&](int i) { return s_first + (tile0 + i) / P.n_tiles; };
 
@@ -1392,6 +1398,9 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
   P.mix_out = t.mix_out;
   P.sq_out = t.sq_out;
   const int64_t grid = P.n_units < sms ? P.n_units : sms;
+  if (P.n_units >= ((int64_t)1 << 31) || grid > 1024) return HCMIX_ERR_INVALID_ARG;
+  P.units_q = (int)(P.n_units / grid);
+  P.units_r = (int)(P.n_units % grid);
   if (staged) P.tail = 0;
   const hcmix_status st = tf32x3 ? tc::launch_main<true>(mx, mw, P, grid, stream)
                                  : tc::launch_main<false>(mx, mw, P, grid, stream);
