@@ -1398,7 +1398,7 @@ inline hcmix_status tc_launch(const uint16_t* x, int64_t x_stride, const float* 
   P.mix_out = t.mix_out;
   P.sq_out = t.sq_out;
   const int64_t grid = P.n_units < sms ? P.n_units : sms;
-  if (P.n_units >= ((int64_t)1 << 31) || grid > 1024) return HCMIX_ERR_INVALID_ARG;
+  if (P.n_units >= ((int64_t)1 << 31) || grid > 1024) return HCMIX_ERR_UNSUPPORTED;
   P.units_q = (int)(P.n_units / grid);
   P.units_r = (int)(P.n_units % grid);
   if (staged) P.tail = 0;

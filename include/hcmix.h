@@ -35,8 +35,11 @@
  *     device error word in the workspace, read with hc_mix_device_status().
  *   - NaN / Inf inputs propagate per IEEE arithmetic without checks.
  *   - Supported shapes: mix == 24, hc == 4, K a positive multiple of 256 up to
- *     2^24, 0 <= M < 2^31.  Finite |x| < 2^112 and |W| < 2^112 (the exact
- *     limb split of the contraction needs that headroom).
+ *     2^24, 0 <= M < 2^31, and for the tensor-core path fewer than 2^31
+ *     (128-row tile, 256-column slice) units, ceil(M / 128) * (K / 256)
+ *     (HCMIX_ERR_UNSUPPORTED otherwise; x would not fit in device memory long
+ *     before that).  Finite |x| < 2^112 and |W| < 2^112 (the exact limb split of
+ *     the contraction needs that headroom).
  */
 #ifndef HCMIX_H
 #define HCMIX_H
