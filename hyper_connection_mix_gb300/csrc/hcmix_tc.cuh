@@ -180,6 +180,20 @@ static_assert(kNumMma == 3 && kNumA == 3 && kNumD == 3 && kNumTWarps == 12 && kN
               "always holds the chunks of the same two thirds); the accumulate warps are two "
               "halves by unit");
 
+// A CTA's unit i (tile, slice), for loops that visit the units in order.
+struct UnitCursor {
+  int i, tile, slice;
+  __device__ __forceinline__ void advance_to(int to, int n_tiles) {
+    while (i < to) {
+      ++i;
+      if (++tile == n_tiles) {
+        tile = 0;
+        ++slice;
+      }
+    }
+  }
+};
+
 // Parameters of one launch (passed by value as a __grid_constant__).
 struct TcParams {
   int n_tiles;     // 128-row tiles
@@ -710,14 +724,18 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   const int tile0 = (int)(u_begin % n_tiles);
   auto unit_tile = [&](int i) { return (tile0 + i) % P.n_tiles; };
   auto unit_slice = [&](int i) { return s_first + (tile0 + i) / P.n_tiles; };
+  // the same for loops that visit the units in order: a cursor moved one unit
+  // at a time (no division per chunk)
+  const UnitCursor cursor0{0, tile0, s_first};
 
-  // x load L fills stage L % kXStages with chunks 2L and 2L + 1 (unit L / 2)
-  auto issue_x_load = [&](int L, uint64_t pol) {
-    const int st = L % kXStages, i = L / 2;
+  // x load L fills stage L % kXStages with chunks 2L and 2L + 1 (unit L / 2,
+  // at which `u` stands)
+  auto issue_x_load = [&](int L, const UnitCursor& u, uint64_t pol) {
+    const int st = L % kXStages;
     const uint32_t full = smem_u32(&bk.full_x[st]);
     mbar_arrive_expect_tx(full, kXBytes);
-    tma_load_3d(x_base + (uint32_t)st * kXBytes, &tmap_x, 0, unit_tile(i) * kTileM,
-                unit_slice(i) * kChunksPerSlice + (L % 2) * kChunksPerStage, full, pol);
+    tma_load_3d(x_base + (uint32_t)st * kXBytes, &tmap_x, 0, u.tile * kTileM,
+                u.slice * kChunksPerSlice + (L % 2) * kChunksPerStage, full, pol);
   };
   // limbs of chunk c of slice s into W buffer (slot, c) by TMA (exact mode)
   auto issue_w_load = [&](int slot, int c, int s, uint64_t pol) {
@@ -826,7 +844,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       }
       {
         const uint64_t pol = l2_policy_evict_first();
-        if (n_loads > 0) issue_x_load(0, pol);
+        if (n_loads > 0) issue_x_load(0, cursor0, pol);
       }
       for (int w = 0; w < kWBufs; ++w) mbar_init(smem_u32(&bk.w_full[w]), 1);
       fence_mbarrier_init();
@@ -901,9 +919,11 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // waits are warp votes and one elected lane issues each MMA and commit.
     const int t = warp - kMmaWarp0;
     bool ok = true;
+    UnitCursor u = cursor0;
     for (int k = t; ok && k < n_chunks; k += kNumMma) {
       const int i = k / kChunksPerSlice, c = k % kChunksPerSlice;
-      const int j = unit_slice(i) - s_first, slot = j % kSlots;
+      u.advance_to(i, P.n_tiles);
+      const int j = u.slice - s_first, slot = j % kSlots;
       bool got = mbar_wait(smem_u32(&bk.mma_ready[t]), (uint32_t)(k / kNumMma) & 1u, abort_flag,
                            kWaitLimitNs);
       got = got && mbar_wait(smem_u32(&bk.w_full[slot * kChunksPerSlice + c]),
@@ -930,15 +950,17 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // load
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
+      UnitCursor u = cursor0;
       int L = 1;
       for (; L < n_loads; ++L) {
         const int st = L % kXStages;
+        u.advance_to(L / 2, P.n_tiles);
         if (L >= kXStages && !mbar_wait(smem_u32(&bk.empty_x[st]), (uint32_t)(L / kXStages - 1) & 1u, abort_flag,
                        kWaitLimitNs)) {
           fail(bk, P.err);
           break;
         }
-        issue_x_load(L, pol);
+        issue_x_load(L, u, pol);
       }
       // drain: the loads still in flight complete before the CTA can exit
       for (int j = max(0, min(L, n_loads) - kXStages); j < min(L, n_loads); ++j)
