@@ -984,6 +984,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t a_col = tmem + (uint32_t)tt * kACols;
+    const uint32_t row_sw = (uint32_t)row * kRowBytes + ((uint32_t)(row & 7) << 4);
     uint32_t cd_par = 0;  // parity of the next phase of chunk_done[s][h]: bit (s / 3) * 2 + h
     bool ok = true;
     for (int k = tt; k < n_chunks; k += kNumA) {
@@ -993,12 +994,15 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                              (uint32_t)(L / kXStages) & 1u, abort_flag,
                                              kWaitLimitNs));
       if (!ok) break;
+      // the row's 16-byte piece p sits at piece p ^ (row & 7) of its 128-byte
+      // row; the row starts on a 128-byte boundary, so that address is
+      // (row start + (row & 7) * 16) ^ p * 16
       const uint32_t xt = x_base + (uint32_t)st * kXBytes + (uint32_t)(k % kChunksPerStage) * kXChunkBytes +
-                          (uint32_t)row * kRowBytes;
+                          row_sw;
       uint32_t xw[32];
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {  // the row's 16-byte pieces at their swizzled places
-        const uint4 v = lds128(xt + ((uint32_t)(p ^ (row & 7)) << 4));
+      for (int p = 0; p < 8; ++p) {
+        const uint4 v = lds128(xt ^ ((uint32_t)p << 4));
         xw[4 * p] = v.x; xw[4 * p + 1] = v.y; xw[4 * p + 2] = v.z; xw[4 * p + 3] = v.w;
       }
       // the row is in registers: this warp's part of the stage is released
