@@ -108,12 +108,18 @@ def workspace_bytes(M: int, K: int, mix: int = MIX) -> int:
     return int(lib().hc_mix_workspace_bytes(M, K, mix))
 
 
+HEADER_BYTES = 256  # the workspace's device error word and grid-barrier counter
+
+
 def alloc_workspace(M: int, K: int, device=None) -> torch.Tensor:
-    """Zeroed workspace (uint8) sized for M rows; torch's allocator aligns it to 512 B."""
+    """Workspace (uint8) sized for M rows, its header zeroed (the rest is
+    written before it is read); torch's allocator aligns it to 512 B."""
     n = workspace_bytes(M, K)
     if n == 0:
         raise HcMixError(3, "workspace_bytes")
-    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    ws[:HEADER_BYTES].zero_()
+    return ws
 
 
 def _check_x(x: torch.Tensor) -> None:

@@ -101,9 +101,10 @@ typedef enum {
 } hcmix_path;
 
 /* Bytes of device workspace that hc_mix_stats / hc_mix_fused need for M rows.
- * The workspace must be 256-byte aligned and zeroed once before its first use
- * (its first 256 bytes hold the device error word); after that every call
- * writes what it reads, so no per-call clearing is needed.  A workspace sized
+ * The workspace must be 256-byte aligned, and its first 256 bytes (the device
+ * error word and the grid barrier's counter) zeroed once before its first use;
+ * the rest needs no initialising, and every call writes what it reads, so no
+ * per-call clearing is needed.  A workspace sized
  * for M rows serves any smaller M.  Calls that share a workspace must not
  * overlap on the GPU (issue them on one stream).  Returns 0 for unsupported
  * (K, mix). */
