@@ -159,6 +159,16 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned 
 __device__ __forceinline__ void red_add_release_gpu_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+// Atomic add at GPU scope, acquire and release: publishes this thread's (and,
+// through a preceding CTA barrier, its CTA's) writes and sees those of every
+// thread whose release add came before it.  Returns the old value.
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu_u64(unsigned long long* p,
+                                                                     unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v)
+               : "memory");
+  return old;
+}
 
 // Named barrier `id` (1..15) over `count` threads of whole warps.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {

@@ -157,6 +157,7 @@ struct Bookkeeping {
   unsigned long long gbar_base;  // the grid barrier's counter before this CTA arrived, rounded down
   int abort;
   int never;  // stays 0: the abort flag of waits that must not be cut short
+  int tail_owner;  // one row group: this CTA's arrival completed the count
 };
 
 static_assert(kDCol0 + kNumD * kDCols<false> <= kTmemCols &&
@@ -517,9 +518,12 @@ __device__ __forceinline__ void fail(Bookkeeping& bk, uint32_t* err) {
 // resident (cooperative launch).  Returns false when the wait ran out.
 constexpr unsigned long long kBarrierQuantum = 1024;  // above any grid size
 
+__device__ __forceinline__ unsigned long long grid_barrier_add(int64_t b, int64_t nblocks) {
+  return b == 0 ? 1 + kBarrierQuantum - (unsigned long long)nblocks : 1;
+}
 __device__ __forceinline__ bool grid_barrier(unsigned long long* counter, unsigned long long base,
                                              int64_t b, int64_t nblocks, uint64_t limit_ns) {
-  sm100::red_add_release_gpu_u64(counter, b == 0 ? 1 + kBarrierQuantum - (unsigned long long)nblocks : 1);
+  sm100::red_add_release_gpu_u64(counter, grid_barrier_add(b, nblocks));
   const unsigned long long target = base + kBarrierQuantum;
   const uint64_t t0 = sm100::global_timer_ns();
   for (uint32_t i = 0; sm100::ld_acquire_gpu_u64(counter) < target; ++i) {
@@ -1219,6 +1223,26 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     tmem_dealloc(tmem, kTmemCols);
   }
   if (P.tail == 0) return;
+
+  if (P.M <= 8) {
+    // ---- one row group (decode sizes): no CTA waits.  Each adds its share
+    // to the same counter with one acquire-release atomic; the CTA whose add
+    // completes the launch's quantum has seen every other CTA's partials and
+    // runs the whole tail, the others are done.
+    if (threadIdx.x == 0) {
+      const unsigned long long add = grid_barrier_add(b, G);
+      const unsigned long long old = atom_add_acq_rel_gpu_u64(P.gbar, add);
+      bk.tail_owner = old + add == bk.gbar_base + kBarrierQuantum;
+    }
+    cta_barrier();
+    if (!bk.tail_owner) return;
+    tail_params(P, smem);
+    const TailPlan T(P, G - 1, G);  // the plan of the CTA that holds the only group
+    if (threadIdx.x == 0) tail_start(P, T, smem, bk.tail_bar);
+    cta_barrier();
+    tc_tail(P, T, smem, bk.tail_bar, never);
+    return;
+  }
 
   // ---- tail: once every CTA's partials are stored (grid barrier) this CTA
   // adds the slices of its rows in slice order and runs the epilogue; the x
