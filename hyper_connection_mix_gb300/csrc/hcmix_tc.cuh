@@ -628,6 +628,17 @@ __device__ __forceinline__ void tail_start(const TcParams& P, const TailPlan& T,
   }
 }
 
+// A shared-memory load for the tail's slice adds.  Not volatile, so that the
+// compiler issues a batch of them back to back; the memory clobber keeps each
+// after the wait for its copy (a volatile form made the compiler treat the
+// kernel's main loops less well, 2.5 µs slower; plain C++ loads were issued
+// one at a time, each paying the shared-memory latency).
+__device__ __forceinline__ float lds_f32_batch(uint32_t addr) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void tc_tail(const TcParams& P, const TailPlan& T, uint8_t* tb,
                                         uint64_t* tbar, const volatile int* never) {
   using namespace sm100;
@@ -656,16 +667,16 @@ __device__ __forceinline__ void tc_tail(const TcParams& P, const TailPlan& T, ui
           record_device_error(P.err, kDevWaitTimeout);
         if (adder) {
           // slice s of value j of row r8 at ((s 25 + j) R + r8); eight loads
-          // at a time, then their adds in slice order (plain loads: the
-          // compiler issues them together)
+          // at a time, then their adds in slice order
           const float* v0 = reinterpret_cast<const float*>(tb + (size_t)slot * kTailSlotBytes) +
                             (j << gs) + r8;
           const int cnt = min(T.per_piece, T.ns - p * T.per_piece);
           int s = 0;
           for (; s + 8 <= cnt; s += 8) {
             float v[8];
+            const uint32_t va = sm100::smem_u32(v0 + s * vstride);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = v0[(s + u) * vstride];
+            for (int u = 0; u < 8; ++u) v[u] = lds_f32_batch(va + (uint32_t)(u * vstride) * 4u);
 #pragma unroll
             for (int u = 0; u < 8; ++u) tot = __fadd_rn(tot, v[u]);
           }
