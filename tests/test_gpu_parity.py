@@ -251,6 +251,27 @@ def test_device_status_clean_after_runs(path):
     assert binding.hc_mix_device_status(ws) == 0
 
 
+@pytest.mark.parametrize("M,K", [(1, 512), (3, 512), (8, 768), (130, 1024)])
+def test_workspace_needs_only_its_header_zeroed(path, M, K):
+    """The workspace contract asks only for its 256-byte header to be zeroed:
+    with every other byte set to 0xFF (a NaN pattern in every fp32 slot), the
+    fused call still gives the oracle's results and no device error, for a
+    single row group (the tail run by the last CTA to arrive) and for several
+    groups with a ragged last tile."""
+    x, W, sc, bs = hi.make_x(M, K=K), hi.make_w(K=K), hi.make_scale(), hi.make_base()
+    want = oracle.fused(x, W, sc, bs, threads=THREADS)
+    ws = binding.alloc_workspace(M, K)
+    ws[binding.HEADER_BYTES:].fill_(0xFF)
+    out = binding.hc_mix_fused(dev_x(x), dev(W), dev(sc), dev(bs), want_stats=True, workspace=ws,
+                               path=path)
+    torch.cuda.synchronize()
+    got = [o.cpu().numpy() for o in out]
+    assert_epilogue_close(got[:3], want[:3], f"M={M}")
+    assert_mix_close(got[3], want[3], f"M={M}")
+    assert np.array_equal(got[4], want[4]), f"M={M}: sq"
+    assert binding.hc_mix_device_status(ws) == 0
+
+
 def test_small_batches_reuse_one_workspace(path):
     """Decode-sized calls that share one workspace give the oracle's results
     every time, with and without the statistics, and leave no device error."""
