@@ -235,6 +235,34 @@ def test_sinkhorn_row_below_the_normal_range(path):
     check_all(x, hi.make_w(K=K), hi.make_scale(), bs, path, "subnormal comb row")
 
 
+def test_nonfinite_inputs_propagate(path):
+    """A NaN or an infinity in a row of x carries into that row's outputs (each
+    output non-finite where the oracle's is), the other rows are unaffected,
+    and the call ends cleanly."""
+    K = 1024
+    x, W, sc, bs = hi.make_x(20, K=K), hi.make_w(K=K), hi.make_scale(), hi.make_base()
+    bf16_nan, bf16_inf = np.uint16(0x7FC0), np.uint16(0x7F80)
+    x[3, 100] = bf16_nan
+    x[11, 7] = bf16_inf
+    want = oracle.fused(x, W, sc, bs, threads=THREADS)
+    ws = binding.alloc_workspace(20, K)
+    out = binding.hc_mix_fused(dev_x(x), dev(W), dev(sc), dev(bs), want_stats=True, workspace=ws,
+                               path=path)
+    torch.cuda.synchronize()
+    got = [o.cpu().numpy() for o in out]
+    bad = [3, 11]
+    good = [r for r in range(20) if r not in bad]
+    for name, g, o in zip(("pre", "post", "comb", "mix", "sq"), got, want):
+        for r in bad:
+            assert not np.all(np.isfinite(o[r])), f"the oracle's {name} of row {r} is finite"
+            assert not np.any(np.isfinite(g[r]) & ~np.isfinite(o[r])), \
+                f"{name} row {r}: finite where the oracle is not"
+    assert_epilogue_close([g[good] for g in got[:3]], [o[good] for o in want[:3]], "finite rows")
+    assert_mix_close(got[3][good], want[3][good], "finite rows")
+    assert np.array_equal(got[4][good], want[4][good]), "finite rows: sq"
+    assert binding.hc_mix_device_status(ws) == 0
+
+
 def test_empty_batch_is_a_no_op(path):
     x = torch.zeros(0, 256, dtype=torch.bfloat16, device="cuda")
     W = torch.zeros(24, 256, dtype=torch.float32, device="cuda")
