@@ -29,7 +29,8 @@ PATHS = {"auto": 0, "simt": 1, "tc": 2, "simt_fullk": 3, "tc_tf32x3": 4, "tc_sta
 EXPORTS = ("hc_mix_workspace_bytes", "hc_mix_stats", "hc_mix_sinkhorn", "hc_mix_fused",
            "hc_mix_stats_ex", "hc_mix_fused_ex", "hc_mix_contract_ex", "hc_mix_auto_path",
            "hc_mix_device_status", "hc_mix_status_string", "hc_mix_fused_noalloc",
-           "hc_mix_packed_w_bytes", "hc_mix_pack_w", "hc_mix_fused_packed")
+           "hc_mix_noalloc_device_status", "hc_mix_packed_w_bytes", "hc_mix_pack_w",
+           "hc_mix_fused_packed")
 
 
 class HcMixError(RuntimeError):
@@ -72,6 +73,8 @@ def lib() -> ctypes.CDLL:
             L.hc_mix_fused_noalloc.restype = I
             L.hc_mix_fused_noalloc.argtypes = [P, I64, P, I64, I64, I64, I, I, P, P, I, F, F,
                                                P, P, P, P, P, P]
+            L.hc_mix_noalloc_device_status.restype = I
+            L.hc_mix_noalloc_device_status.argtypes = [P]
             L.hc_mix_packed_w_bytes.restype = S
             L.hc_mix_packed_w_bytes.argtypes = [I64, I]
             L.hc_mix_pack_w.restype = I

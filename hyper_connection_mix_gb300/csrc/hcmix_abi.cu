@@ -379,6 +379,9 @@ hcmix_status hc_mix_fused_noalloc(const void* x, int64_t x_stride, const float* 
                                   int sinkhorn_iters, float rms_eps, float hc_eps, float* pre,
                                   float* post, float* comb, float* mix_out, float* sq_out,
                                   void* stream) {
+  // the static array is the workspace of an ordinary hc_mix_fused call (zero at
+  // load, so its header starts as a workspace's must).  The arguments are
+  // checked first, before any CUDA call.
   hcmix_status st = check_shape(M, K, mix);
   if (st != HCMIX_OK) return st;
   st = check_epilogue_args(M, K, hc, hc_scale, hc_base, sinkhorn_iters, pre, post, comb);
@@ -388,26 +391,20 @@ hcmix_status hc_mix_fused_noalloc(const void* x, int64_t x_stride, const float* 
   if (x_stride < K || w_stride < K) return HCMIX_ERR_INVALID_ARG;
   if (!aligned(x, 16) || (x_stride * 2) % 16 != 0) return HCMIX_ERR_ALIGNMENT;
   if (!aligned(W, 16) || (w_stride * 4) % 16 != 0) return HCMIX_ERR_ALIGNMENT;
-  const int64_t n_slices = K / kSlice;
-  const int64_t Mpad = (M + 127) / 128 * 128;
-  const size_t need = (size_t)n_slices * kPartStride * (size_t)Mpad * 4;
-  if (need > kStaticScratchBytes) return HCMIX_ERR_WORKSPACE;
+  if (workspace_layout(M, K).total > kStaticScratchBytes) return HCMIX_ERR_WORKSPACE;
   void* scratch = nullptr;
   st = static_scratch_address(&scratch);
   if (st != HCMIX_OK) return st;
-  float* part = static_cast<float*>(scratch);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid((unsigned)((M + kSimtRows - 1) / kSimtRows), (unsigned)n_slices);
-  if (simt_smem_attributes() != HCMIX_OK) return HCMIX_ERR_CUDA;
-  hcmix_simt_slice_kernel<<<grid, kSimtThreads, kSimtSmemBytes, s>>>(
-      static_cast<const uint16_t*>(x), x_stride, W, w_stride, (int)M, (int)Mpad, part);
-  st = launch_status();
+  return hc_mix_fused_ex(x, x_stride, W, w_stride, M, K, mix, hc, hc_scale, hc_base,
+                         sinkhorn_iters, rms_eps, hc_eps, pre, post, comb, mix_out, sq_out,
+                         scratch, kStaticScratchBytes, stream, HCMIX_PATH_AUTO);
+}
+
+hcmix_status hc_mix_noalloc_device_status(void* stream) {
+  void* scratch = nullptr;
+  const hcmix_status st = static_scratch_address(&scratch);
   if (st != HCMIX_OK) return st;
-  const float inv_k = (float)(1.0 / (double)K);
-  hcmix_reduce_kernel<<<(unsigned)((M + kReduceRows - 1) / kReduceRows), kReduceThreads, 0, s>>>(
-      part, (int)n_slices, (int)Mpad, (int)M, inv_k, hc_scale, hc_base, sinkhorn_iters, rms_eps,
-      hc_eps, pre, post, comb, mix_out, sq_out, 1);
-  return launch_status();
+  return hc_mix_device_status(scratch, stream);
 }
 
 hcmix_status hc_mix_device_status(void* workspace, void* stream) {

@@ -197,11 +197,14 @@ hcmix_path hc_mix_auto_path(int64_t M);
  * Instead of a caller workspace it uses a fixed scratch array of
  * HC_MIX_STATIC_SCRATCH_BYTES (2 MiB) that the library defines in device
  * memory; every GPU that loads libhcmix.so holds that array until the process
- * exits.  It runs the CUDA-core split-K kernel (HCMIX_PATH_SIMT) and allocates
- * nothing: no cudaMalloc, no cudaFree, no allocating library call.
- *   - Limit: ceil(M / 128) * 128 * (K / 256) * 25 * 4 bytes must fit the
- *     scratch, i.e. M <= 256 at K = 20480.  Larger problems return
- *     HCMIX_ERR_WORKSPACE before anything is launched.
+ * exits.  It runs hc_mix_fused's default path (HCMIX_PATH_AUTO: the
+ * tensor-core kernel on GB300) with that array as its workspace, and
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Limit: hc_mix_workspace_bytes(M, K, mix) must fit the scratch, i.e.
+ *     M <= 256 at K = 20480.  Larger problems return HCMIX_ERR_WORKSPACE
+ *     before anything is launched.
+ *   - The array's header holds the device error word of these calls:
+ *     hc_mix_noalloc_device_status reads (and clears) it.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address once and keeps it for later calls; make that
  *     first call before any stream capture starts on that device.  The kept
@@ -222,6 +225,13 @@ hcmix_status hc_mix_fused_noalloc(const void* x, int64_t x_stride, const float* 
                                   int sinkhorn_iters, float rms_eps, float hc_eps,
                                   float* pre, float* post, float* comb,
                                   float* mix_out, float* sq_out, void* stream);
+
+/* The device error word of hc_mix_fused_noalloc's calls on the current
+ * device (the kernel status of hc_mix_device_status, read from the fixed
+ * scratch array): synchronises `stream`, returns HCMIX_OK when clean or the
+ * recorded error, and clears it.  HCMIX_ERR_CUDA if the array's address cannot
+ * be looked up (see the notes on hc_mix_fused_noalloc). */
+hcmix_status hc_mix_noalloc_device_status(void* stream);
 
 /* Synchronises `stream`, then reads and clears the device error word that
  * kernels set in `workspace` when a bounded wait runs out.  HCMIX_OK when clean,

@@ -4,8 +4,8 @@ forbids later cudaMalloc, or a plug-in whose host framework owns every device
 allocation).  It keeps its scratch in a fixed 2 MiB device array inside the
 library instead of a caller workspace.
 
-Checked through the C ABI against hc_mix_fused's CUDA-core path (which uses a
-caller workspace) on two calls in a row.  Both run the same kernels with the
+Checked through the C ABI against hc_mix_fused's default path (which uses a
+caller workspace) on two calls in a row.  Both run the same kernel with the
 same arithmetic in the same order, so every output must be bit-identical; a
 scratch-layout slip would show up as a changed bit before it shows up as a
 tolerance failure.  This file is collected last; it must pass alone in a fresh
@@ -50,7 +50,7 @@ def test_noalloc_matches_workspace_entry_point_twice(M, K):
     W, sc, bs = hi.make_w(K=K), hi.make_scale(), hi.make_base()
     xt = _dev_x(x)
     Wt, sct, bst = (torch.from_numpy(a).cuda() for a in (W, sc, bs))
-    ref = binding.hc_mix_fused(xt, Wt, sct, bst, want_stats=True, path="simt")
+    ref = binding.hc_mix_fused(xt, Wt, sct, bst, want_stats=True, path="auto")
     for call in range(2):
         # a different input between the two calls: the second call must not see
         # anything the first one left in the shared scratch
@@ -61,6 +61,7 @@ def test_noalloc_matches_workspace_entry_point_twice(M, K):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32)), f"call {call}: {name}"
         other = _dev_x(hi.make_x(M, K=K, seed=7))
         assert _noalloc(L, other, Wt, sct, bst, _outs(M), stream) == 0
+    assert L.hc_mix_noalloc_device_status(stream) == 0
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
