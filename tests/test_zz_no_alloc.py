@@ -42,7 +42,7 @@ def _outs(M):
             torch.empty(M, device="cuda"))
 
 
-@pytest.mark.parametrize("M,K", [(256, 20480), (37, 20480), (129, 1024)])
+@pytest.mark.parametrize("M,K", [(256, 20480), (37, 20480), (129, 1024), (1, 20480), (4, 1024)])
 def test_noalloc_matches_workspace_entry_point_twice(M, K):
     L = binding.lib()
     stream = torch.cuda.current_stream().cuda_stream
