@@ -153,6 +153,7 @@ struct Bookkeeping {
   uint64_t w_stage;  // the fp32 W of the first two slices has landed in slot 1 (TMA)
   uint64_t drain[kNumMma];
   uint64_t tail_bar[6];  // the tail's copy slots (kTailSlots)
+  uint64_t refill_done[2];  // per accumulate half: its four warps have converted a refilled slot
   uint32_t tmem_base;
   unsigned long long gbar_base;  // the grid barrier's counter before this CTA arrived, rounded down
   int abort;
@@ -163,7 +164,8 @@ struct Bookkeeping {
 static_assert(kDCol0 + kNumD * kDCols<false> <= kTmemCols &&
                   kDCol0 + kNumD * kDCols<true> <= kTmemCols, "TMEM budget");
 static_assert(sizeof(Bookkeeping) <= 1024, "bookkeeping area");
-static_assert(3 + 3 + 6 + 12 + 6 < 31, "one barrier (pair) per lane of the initialising warp");
+static_assert(3 + 3 + 6 + 12 + 6 <= 30,
+              "one barrier (pair) per lane of the initialising warp; lanes 30 and 31 do the rest");
 static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of one unit");
 static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynamic shared memory");
 static_assert(Mode<false>::kBBytes % 1024 == 0 && Mode<true>::kBlockBytes % 1024 == 0,
@@ -890,6 +892,8 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the four accumulate warps of the chunk
     } else if (lane < kNumMma + kNumA + 2 * kNumD + 2 * kNumSq + kTailSlots) {
       mbar_init(smem_u32(&bk.tail_bar[lane - kNumMma - kNumA - 2 * kNumD - 2 * kNumSq]), 1);
+    } else if (lane == 30) {
+      for (int h = 0; h < 2; ++h) mbar_init(smem_u32(&bk.refill_done[h]), 4);  // the half's four warps
     } else if (lane == 31) {
       bk.abort = 0;
       bk.never = 0;
@@ -1102,16 +1106,30 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
     // A CTA with more than two slices reuses the slots: once a half has read
     // the last chunk of slice j - 2, every MMA of that slice is complete, and
-    // that half fills slice j's slot (j % 2) before reading on.
+    // that half fills slice j's slot (j % 2) before reading on.  Each of its
+    // four warps arrives on refill_done[dh] once its share is converted; the
+    // half's first warp alone waits there (a bounded wait: a warp that gave
+    // up on an earlier wait cannot hold the others) and marks the slot full.
+    // Refills of a half lie at least two units apart and no warp of the half
+    // runs more than three chunks ahead of another (the D ring), so the first
+    // warp has waited for every phase before the next one completes.
+    uint32_t refill_par = 0;  // parity of the next phase of refill_done[dh]
     auto refill = [&](int jn) {
       const int slot = jn % kSlots;
       if (P.w_src != nullptr) {
         convert_slice(jn, htid, 4 * 32);
         fence_proxy_async_smem();
-        named_bar_sync(2 + dh, 4 * 32);
-        if (htid == 0)
-          for (int c = 0; c < kChunksPerSlice; ++c)
-            mbar_arrive(smem_u32(&bk.w_full[slot * kChunksPerSlice + c]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bk.refill_done[dh]));
+        if (htid < 32) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.refill_done[dh]), refill_par,
+                                                 abort_flag, kWaitLimitNs)))
+            fail(bk, P.err);
+          else if (htid == 0)
+            for (int c = 0; c < kChunksPerSlice; ++c)
+              mbar_arrive(smem_u32(&bk.w_full[slot * kChunksPerSlice + c]));
+        }
+        refill_par ^= 1u;
       } else if constexpr (!kTf32) {
         if (htid == 0)
           for (int c = 0; c < kChunksPerSlice; ++c)

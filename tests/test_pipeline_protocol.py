@@ -62,6 +62,8 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     # d_full[b * 2 + h]: D buffer b holds a chunk of accumulate half h
     d_full, w_full = mk("d_full", 1, 2 * N_D), mk("w_full", 1, 4 * SLOTS)
     dconv = Bar(8, "dconv")
+    # refill_done[h]: the half's four warps have converted a refilled slot
+    refill_done = mk("refill_done", 4, 2)
     errors, pipe, tma = [], [], []
     # progress, for the buffer checks
     x_read = [0] * nld          # transform warps that have read x load L
@@ -141,6 +143,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                         w_full[4 * j + c].arrive()
         seen = [0] * N_D  # phases of d_full[b * 2 + dh] waited for so far
         sq_seen = [0] * N_SQ  # phases of sq_full[s * 2 + dh] waited for so far
+        rf_seen = 0  # phases of refill_done[dh] waited for so far (warp q == 0)
         for i in range(dh, n, 2):
             for c in range(4):
                 k = 4 * i + c
@@ -158,10 +161,21 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                 chunk_done[s_ * 2 + dh].arrive()
                 mma_ready[b].arrive()  # D buffer b free for chunk k + 3
             j = sl[i] - s_first
-            if j + SLOTS < n_sl and (i == n - 1 or sl[i + 1] != sl[i]) and q == 0:
-                slice_done.add(sl[i])
-                for c in range(4):  # refill: slice j + 2 into slot j % 2
-                    w_full[((j + SLOTS) % SLOTS) * 4 + c].arrive()
+            if j + SLOTS < n_sl and (i == n - 1 or sl[i + 1] != sl[i]):
+                # refill: slice j + 2 into slot j % 2.  Converted in-kernel: every
+                # warp of the half arrives on refill_done, the first waits there
+                # and then marks the slot full; prepacked limbs: the first warp
+                # issues the loads
+                if not packed:
+                    yield None
+                    refill_done[dh].arrive()
+                if q == 0:
+                    if not packed:
+                        yield from wait(refill_done[dh], rf_seen, f"D{dh}{q} refill {j + SLOTS}")
+                        rf_seen += 1
+                    slice_done.add(sl[i])
+                    for c in range(4):
+                        w_full[((j + SLOTS) % SLOTS) * 4 + c].arrive()
 
     if packed:
         for c in range(4 * min(SLOTS, n_sl)):
