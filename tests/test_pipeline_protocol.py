@@ -71,6 +71,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     d_read = [0] * nck          # accumulate warps that have read D of chunk k
     sq_read = [0] * nck         # accumulate warps that have read the sum of squares of chunk k
     slice_done = set()          # slices whose every MMA completed (W slot free)
+    converted = {}              # refilled slice -> warps of its half that have converted their share
 
     def wait(bar, phase, who):
         parity = phase & 1
@@ -168,11 +169,14 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                 # issues the loads
                 if not packed:
                     yield None
+                    converted[j + SLOTS] = converted.get(j + SLOTS, 0) + 1
                     refill_done[dh].arrive()
                 if q == 0:
-                    if not packed:
+                    if not packed and PLANTED != "refill_no_wait":
                         yield from wait(refill_done[dh], rf_seen, f"D{dh}{q} refill {j + SLOTS}")
                         rf_seen += 1
+                    check(packed or converted.get(j + SLOTS) == 4,
+                          f"slot of slice {j + SLOTS} marked full before its conversion was done")
                     slice_done.add(sl[i])
                     for c in range(4):
                         w_full[((j + SLOTS) % SLOTS) * 4 + c].arrive()
@@ -238,17 +242,21 @@ def test_protocol_sound_and_deadlock_free(M, K):
                 assert not errs, f"M={M} K={K} units {ub}+{n} seed {seed}: {errs[:3]}"
 
 
-@pytest.mark.parametrize("mistake", ["wrong_a_buffer", "d_full_by_buffer"])
+@pytest.mark.parametrize("mistake", ["wrong_a_buffer", "d_full_by_buffer", "refill_no_wait"])
 def test_model_catches_planted_mistakes(mistake):
     """The checks have teeth: a transform third that waits on another third's
-    A barrier, or accumulate halves that share one D barrier per buffer (each
-    then sees only some of its phases), are reported (an early return, a buffer rewritten too soon, or
-    the deadlock they lead to)."""
+    A barrier, accumulate halves that share one D barrier per buffer (each
+    then sees only some of its phases), or a refilled W slot marked full by
+    the half's first warp without waiting for the other three, are reported
+    (an early return, a buffer rewritten or used too soon, or the deadlock
+    they lead to)."""
     global PLANTED
     PLANTED = mistake
     found = False
+    # the refill needs CTAs with more than two slices: M = 130, K = 131072
+    ctas = grid_ctas(130, 131072)[:8] if mistake == "refill_no_wait" else grid_ctas(4096, 20480)[:8]
     try:
-        for ub, n, nt in grid_ctas(4096, 20480)[:8]:
+        for ub, n, nt in ctas:
             for seed in range(8):
                 try:
                     found = found or bool(run_cta(ub, n, nt, seed))
