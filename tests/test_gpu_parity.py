@@ -94,6 +94,17 @@ def test_ragged_rows_several_tiles(path, M):
               f"M={M}")
 
 
+@pytest.mark.parametrize("M,K", [(1, 40960), (3, 9472), (9, 2560), (127, 5120), (129, 768),
+                                 (513, 20480), (1000, 1280), (2049, 2048), (6, 122880)])
+def test_irregular_shapes(path, M, K):
+    """Shapes off the workloads' grid: tile counts just above and below a
+    multiple of 128 rows, slice counts that split unevenly over the CTAs
+    (37, 5, 3 slices), more units than CTAs, and few rows with many slices,
+    where each CTA refills its W slots."""
+    check_all(hi.make_x(M, K=K, seed=M + K), hi.make_w(K=K), hi.make_scale(), hi.make_base(),
+              path, f"M={M} K={K}")
+
+
 def test_config_m16(path):
     check_all(hi.make_x(16), hi.make_w(), hi.make_scale(), hi.make_base(), path, "M=16")
 
