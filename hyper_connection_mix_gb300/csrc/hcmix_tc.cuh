@@ -26,14 +26,14 @@
 //     quadrant): third t takes the chunks with k % 3 == t.  Each thread reads
 //     its row of the chunk from the x stage, sums its squares by the page's
 //     fixed tree, splits x into the limbs x0 (grid-aligned) and x1 = x - x0
-//     and stores both into TMEM A buffer t (x as fp32 in tf32x3 mode); the
-//     chunk's sum of squares goes to a shared-memory slot;
+//     and stores both into TMEM A buffer t (x as fp32 in tf32x3 mode), and
+//     the chunk's sum of squares into TMEM column 480 + k % 6;
 //   * warps 16..23, the accumulate warps, two halves of four (one per
 //     quadrant): half dh takes the units with i % 2 == dh, so that two
 //     units' reads are in flight at once.  They read D (TMEM round trips of
-//     4 x 8 columns), form the chunk dots fl32(top + ((r1 + r2) + r3)), add
-//     them into the slice totals (chunks in order, from zero), add the
-//     chunk's sum of squares likewise, and store the 24 + 1 slice totals per
+//     4 x 8 columns, and the sum-of-squares column), form the chunk dots
+//     fl32(top + ((r1 + r2) + r3)), add them into the slice totals (chunks in
+//     order, from zero), add the chunk's sum of squares likewise, and store the 24 + 1 slice totals per
 //     row to the workspace partials at the end of the unit.  Before that they
 //     convert the staged fp32 W into the exact bf16 limbs (or the tf32x3 big
 //     / small parts) in shared memory, and they refill a slot when the CTA
@@ -43,8 +43,13 @@
 // written, MMAs issued and completed, rewritten; D buffer: MMAs completed,
 // read, next MMAs issued) spans fewer than three chunks.  Every mbarrier wait
 // is by a waiter that has seen the barrier's previous phase, as a parity wait
-// needs: each A buffer, D buffer (per accumulate half), sum slot (per half)
-// and x stage slot has fixed waiters that see every phase.
+// needs: each A buffer, D buffer (per accumulate half) and x stage slot has
+// fixed waiters that see every phase.  The sums of squares need no barrier of
+// their own: column 480 + k % 6 is written with chunk k's A (before its MMAs
+// are issued) and read with its D (after they complete), and it is written
+// again for chunk k + 6 only after the MMAs of chunk k + 3 completed, which
+// were issued only after the accumulate warps had read chunk k's D, and with
+// it the column.
 //
 // Tail (same kernel): once every CTA has stored its partials (a grid-wide
 // barrier; the launch is cooperative, so every CTA is resident), CTA b adds
@@ -79,7 +84,7 @@ constexpr int kXStages = 3;        // x stages in flight
 constexpr int kChunksPerStage = 2;  // an x stage holds two chunks of a tile (one 32 KB load)
 constexpr int kNumA = 3;   // TMEM A buffers: chunk k uses A buffer k % 3 (transform third k % 3)
 constexpr int kNumD = 3;   // TMEM D buffers: chunk k uses D buffer k % 3
-constexpr int kNumSq = 6;  // sum-of-squares slots (shared memory): chunk k uses slot k % 6
+constexpr int kNumSq = 6;  // sum-of-squares TMEM columns: chunk k uses kSqCol0 + k % 6
 constexpr int kSlots = 2;  // W slots: a CTA's consecutive slices alternate between them
 constexpr int kWBufs = kSlots * kChunksPerSlice;
 constexpr int kMmaWarp0 = 0, kTmemWarp = 1;
@@ -104,6 +109,7 @@ constexpr uint32_t kLimbRowOffset = kMix;                     // limbs occupy B 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACols = 64;  // exact: x0 and x1, 32 columns each; tf32x3: 64 fp32 x
 constexpr uint32_t kDCol0 = kNumA * kACols;  // first D column
+constexpr uint32_t kSqCol0 = 480;             // the sums of squares, past the D buffers
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 500000000ull;
 
@@ -135,9 +141,7 @@ constexpr size_t kXOff = 0;
 template <bool kTf32>
 constexpr size_t kWOff = (size_t)kXStages * kXBytes;
 template <bool kTf32>
-constexpr size_t kSqOff = kWOff<kTf32> + (size_t)kWBufs * Mode<kTf32>::kBBytes;
-template <bool kTf32>
-constexpr size_t kBkOff = kSqOff<kTf32> + (size_t)kNumSq * kTileM * 4;
+constexpr size_t kBkOff = kWOff<kTf32> + (size_t)kWBufs * Mode<kTf32>::kBBytes;
 template <bool kTf32>
 constexpr size_t kSmemBytes = kBkOff<kTf32> + 1024 + 1024;  // bookkeeping + base alignment
 
@@ -146,9 +150,7 @@ struct Bookkeeping {
   uint64_t empty_x[kXStages];
   uint64_t a_empty[kNumA];  // [k % 3]: the MMAs of chunk k are done (A buffer free)
   uint64_t mma_ready[kNumMma];  // chunk k (issuer k % 3): A(k) written and D(k - 3) read
-  uint64_t sq_full[kNumSq * 2];     // [k % 6 * 2 + (k / 4) % 2]: chunk k's sum of squares is in its slot
   uint64_t d_full[kNumD * 2];  // [b * 2 + (k / 4) % 2]: D buffer b holds chunk k, of accumulate half (k / 4) % 2
-  uint64_t chunk_done[kNumSq * 2];  // [k % 6 * 2 + (k / 4) % 2]: the accumulate half has read it
   uint64_t w_full[kWBufs];
   uint64_t w_stage;  // the fp32 W of the first two slices has landed in slot 1 (TMA)
   uint64_t drain[kNumMma];
@@ -161,10 +163,11 @@ struct Bookkeeping {
   int tail_owner;  // one row group: this CTA's arrival completed the count
 };
 
-static_assert(kDCol0 + kNumD * kDCols<false> <= kTmemCols &&
-                  kDCol0 + kNumD * kDCols<true> <= kTmemCols, "TMEM budget");
+static_assert(kDCol0 + kNumD * kDCols<false> <= kSqCol0 &&
+                  kDCol0 + kNumD * kDCols<true> <= kSqCol0 && kSqCol0 + kNumSq <= kTmemCols,
+              "TMEM budget");
 static_assert(sizeof(Bookkeeping) <= 1024, "bookkeeping area");
-static_assert(3 + 3 + 6 + 12 + 6 <= 30,
+static_assert(3 + 3 + 6 + 6 <= 30,
               "one barrier (pair) per lane of the initialising warp; lanes 30 and 31 do the rest");
 static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of one unit");
 static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynamic shared memory");
@@ -715,7 +718,6 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bookkeeping& bk = *reinterpret_cast<Bookkeeping*>(smem + kBkOff<kTf32>);
-  float* sq_buf = reinterpret_cast<float*>(smem + kSqOff<kTf32>);  // [kNumSq][128]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int64_t G = gridDim.x, b = blockIdx.x;
@@ -886,12 +888,8 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       mbar_init(smem_u32(&bk.a_empty[lane - kNumMma]), 1);  // MMA commit
     } else if (lane < kNumMma + kNumA + 2 * kNumD) {
       mbar_init(smem_u32(&bk.d_full[lane - kNumMma - kNumA]), 1);  // MMA commit
-    } else if (lane < kNumMma + kNumA + 2 * kNumD + 2 * kNumSq) {
-      const int q = lane - kNumMma - kNumA - 2 * kNumD;
-      mbar_init(smem_u32(&bk.sq_full[q]), 4);     // the four transform warps of the chunk
-      mbar_init(smem_u32(&bk.chunk_done[q]), 4);  // the four accumulate warps of the chunk
-    } else if (lane < kNumMma + kNumA + 2 * kNumD + 2 * kNumSq + kTailSlots) {
-      mbar_init(smem_u32(&bk.tail_bar[lane - kNumMma - kNumA - 2 * kNumD - 2 * kNumSq]), 1);
+    } else if (lane < kNumMma + kNumA + 2 * kNumD + kTailSlots) {
+      mbar_init(smem_u32(&bk.tail_bar[lane - kNumMma - kNumA - 2 * kNumD]), 1);
     } else if (lane == 30) {
       for (int h = 0; h < 2; ++h) mbar_init(smem_u32(&bk.refill_done[h]), 4);  // the half's four warps
     } else if (lane == 31) {
@@ -994,21 +992,18 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // complete: earlier, the wait cannot tell p - 2 (same parity) from p and
     // returns at once.  Every wait below follows that rule: with three x stages
     // of two chunks, stage slot L % 3 always holds chunks of the same two
-    // thirds, so this third waits for every phase of the slots it uses;
-    // a_empty[tt] carries only this third's chunks; and chunk_done[s][h] (sum
-    // slot s, accumulate half h) only chunks of slots s that this third
-    // writes, whose phases it tracks bit by bit.
+    // thirds, so this third waits for every phase of the slots it uses; and
+    // a_empty[tt] carries only this third's chunks.
     const int tt = (warp - kFirstTWarp) >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t a_col = tmem + (uint32_t)tt * kACols;
     const uint32_t row_sw = (uint32_t)row * kRowBytes + ((uint32_t)(row & 7) << 4);
-    uint32_t cd_par = 0;  // parity of the next phase of chunk_done[s][h]: bit (s / 3) * 2 + h
     bool ok = true;
     for (int k = tt; k < n_chunks; k += kNumA) {
       const int L = k / kChunksPerStage, st = L % kXStages;
-      const int s = k % kNumSq, dh = (k / kChunksPerSlice) & 1;
+      const int s = k % kNumSq;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.full_x[st]),
                                              (uint32_t)(L / kXStages) & 1u, abort_flag,
                                              kWaitLimitNs));
@@ -1051,18 +1046,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
           xw[t] = bf16x2_sub(xw[t], lo[t]);  // x1, in place
         }
       }
-      // sum slot s is free once the accumulate half of chunk k - 6 has read
-      // it; A buffer tt once the MMAs of chunk k - 3 are done
-      if (k >= kNumSq) {
-        const int hm = ((k - kNumSq) / kChunksPerSlice) & 1, bit = (s / kNumA) * 2 + hm;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.chunk_done[s * 2 + hm]),
-                                               (cd_par >> bit) & 1u, abort_flag, kWaitLimitNs));
-        cd_par ^= 1u << bit;
-        if (!ok) break;
-      }
-      sq_buf[s * kTileM + row] = tsq;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bk.sq_full[s * 2 + dh]));
+      // A buffer tt is free once the MMAs of chunk k - 3 are done; so is sum
+      // column s: the accumulate warps read chunk k - 6's column before they
+      // freed D for chunk k - 3's MMAs
       if (k >= kNumA) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.a_empty[tt]),
                                                (uint32_t)(k / kNumA - 1) & 1u, abort_flag,
@@ -1072,6 +1058,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       tc_fence_after();
       tmem_st32(lanes | a_col, lo);
       tmem_st32(lanes | (a_col + 32), xw);
+      tmem_st1(lanes | (tmem + kSqCol0 + (uint32_t)s), __float_as_uint(tsq));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -1140,10 +1127,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const uint64_t keep = l2_policy_evict_last();  // the tail reads the partials next
-    // the parity of the next phase this half waits for on d_full[b][dh] and
-    // sq_full[s][dh] (this half waits for every phase of those barriers, in
-    // order)
-    uint32_t dpar = 0, sqpar = 0;
+    // the parity of the next phase this half waits for on d_full[b][dh] (this
+    // half waits for every phase of those barriers, in order)
+    uint32_t dpar = 0;
     bool ok = true;
     for (int i = dh; ok && i < n; i += 2) {
       float2 acc[kMix / 2];
@@ -1152,19 +1138,17 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       float sqs = 0.0f;
       for (int c = 0; c < kChunksPerSlice; ++c) {
         const int k = kChunksPerSlice * i + c, b = k % kNumD;
-        // D of chunk k complete, and the chunk's sum of squares in its slot
+        // D of chunk k complete (and with it the chunk's sum of squares)
         const int sl = k % kNumSq;
-        bool got = mbar_wait(smem_u32(&bk.d_full[b * 2 + dh]), (dpar >> b) & 1u, abort_flag,
-                             kWaitLimitNs);
+        const bool got = mbar_wait(smem_u32(&bk.d_full[b * 2 + dh]), (dpar >> b) & 1u,
+                                   abort_flag, kWaitLimitNs);
         dpar ^= 1u << b;
-        got = got && mbar_wait(smem_u32(&bk.sq_full[sl * 2 + dh]), (sqpar >> sl) & 1u, abort_flag,
-                               kWaitLimitNs);
-        sqpar ^= 1u << sl;
         ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_col = tmem + kDCol0 + (uint32_t)b * kDCols<kTf32>;
-        const float tsq = sq_buf[sl * kTileM + row];
+        uint32_t tsq;  // (in hand at the first wait::ld below)
+        tmem_ld1(lanes | (tmem + kSqCol0 + (uint32_t)sl), tsq);
         if constexpr (kTf32) {
           uint32_t dv[kMix];
           tmem_ld16(lanes | d_col, dv);
@@ -1173,7 +1157,6 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(smem_u32(&bk.chunk_done[sl * 2 + dh]));
             mbar_arrive(smem_u32(&bk.mma_ready[b]));  // D buffer b free for chunk k + 3
           }
 #pragma unroll
@@ -1199,7 +1182,6 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
               tc_fence_before();
               __syncwarp();
               if (lane == 0) {
-                mbar_arrive(smem_u32(&bk.chunk_done[sl * 2 + dh]));
                 mbar_arrive(smem_u32(&bk.mma_ready[b]));  // D buffer b free for chunk k + 3
               }
             }
@@ -1214,7 +1196,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
             }
           }
         }
-        sqs = __fadd_rn(sqs, tsq);
+        sqs = __fadd_rn(sqs, __uint_as_float(tsq));
       }
       if (!ok) break;
       const int grow = unit_tile(i) * kTileM + row;

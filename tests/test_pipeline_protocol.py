@@ -3,7 +3,9 @@
 The kernel's roles (the x producer, three thirds of four transform warps by
 chunk, three MMA issuers, two halves of four accumulate warps by unit, the
 W-slot refills) hand chunks to each other through mbarriers whose waits only test the
-parity of the phase they want.  Such a wait is sound only when the waiter
+parity of the phase they want; the chunk's sum of squares travels in a TMEM
+column (k % 6) written with the chunk's A and read with its D, guarded by no
+barrier of its own.  Such a wait is sound only when the waiter
 already knows the phase before it complete; otherwise it cannot tell phase
 p - 2 from phase p and returns early.  This module restates, role by role, the
 waits and arrivals of hyper_connection_mix_gb300/csrc/hcmix_tc.cuh as a model
@@ -12,9 +14,10 @@ wait that returns when the current phase parity differs), runs it under random
 interleavings with the MMAs completing in issue order and the x loads landing
 in any order, and asserts
   * for every wait, that the exact phase it needed had completed;
-  * for every buffer (x stage, TMEM A and D buffers, sum-of-squares slot, W
-    slot), that it is only rewritten once every reader of its previous
-    contents is done;
+  * for every buffer (x stage, TMEM A and D buffers, sum-of-squares column,
+    W slot), that it is only rewritten once every reader of its previous
+    contents is done, and that the sum column read with chunk k's D holds
+    chunk k's value;
   * that every run finishes.
 It is a model of the kernel's protocol, kept beside the kernel; the GPU tests
 check the kernel itself.
@@ -57,8 +60,6 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
         for _ in range(4):
             b.arrive()
     a_empty = mk("a_empty", 1, N_A)  # [k % 3]: chunk k's MMAs done
-    # [k % 6 * 2 + (k / 4) % 2]: sum slot of chunk k filled / read by its accumulate half
-    sq_full, chunk_done = mk("sq_full", 4, 2 * N_SQ), mk("chunk_done", 4, 2 * N_SQ)
     # d_full[b * 2 + h]: D buffer b holds a chunk of accumulate half h
     d_full, w_full = mk("d_full", 1, 2 * N_D), mk("w_full", 1, 4 * SLOTS)
     dconv = Bar(8, "dconv")
@@ -70,6 +71,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     mma_done = set()            # chunks whose MMAs completed
     d_read = [0] * nck          # accumulate warps that have read D of chunk k
     sq_read = [0] * nck         # accumulate warps that have read the sum of squares of chunk k
+    sq_col = {}                 # (column, quadrant) -> the chunk whose sum it holds
     slice_done = set()          # slices whose every MMA completed (W slot free)
     converted = {}              # refilled slice -> warps of its half that have converted their share
 
@@ -96,25 +98,21 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
             yield None
 
     def transform(tt, q):  # the chunks k with k % 3 == tt
-        cd_seen = {}  # phases of chunk_done[s][h] waited for so far
         for k in range(tt, nck, N_A):
             L, st = k // 2, (k // 2) % X_STAGES
-            s_, dh = k % N_SQ, (k // 4) % 2
+            s_ = k % (3 if PLANTED == "sq_col_mod3" else N_SQ)
             yield from wait(full_x[st], L // X_STAGES, f"T{tt}{q} k{k} x")
             yield None
             x_read[L] += 1
             empty_x[st].arrive()
-            if k >= N_SQ:
-                hm = ((k - N_SQ) // 4) % 2
-                key = s_ * 2 + hm
-                yield from wait(chunk_done[key], cd_seen.get(key, 0), f"T{tt}{q} k{k} sq")
-                cd_seen[key] = cd_seen.get(key, 0) + 1
-                check(sq_read[k - N_SQ] == 4, f"sq slot of chunk {k} over an unread one")
-            sq_full[s_ * 2 + dh].arrive()
             if k >= N_A:  # chunk k - 3 (this third's) is done with A buffer tt
                 a = (tt + 1) % N_A if PLANTED == "wrong_a_buffer" else tt
                 yield from wait(a_empty[a], k // N_A - 1, f"T{tt}{q} k{k} A")
                 check(k - N_A in mma_done, f"A buffer of chunk {k} rewritten before the MMAs of {k - N_A} were done")
+            # the A limbs and the sum of squares into TMEM
+            old = sq_col.get((s_, q))
+            check(old is None or sq_read[old] == 4, f"sum column of chunk {k} over chunk {old}'s unread one")
+            sq_col[(s_, q)] = k
             yield None
             mma_ready[k % N_MMA].arrive()
 
@@ -143,7 +141,6 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                     for c in range(4):
                         w_full[4 * j + c].arrive()
         seen = [0] * N_D  # phases of d_full[b * 2 + dh] waited for so far
-        sq_seen = [0] * N_SQ  # phases of sq_full[s * 2 + dh] waited for so far
         rf_seen = 0  # phases of refill_done[dh] waited for so far (warp q == 0)
         for i in range(dh, n, 2):
             for c in range(4):
@@ -152,14 +149,12 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                 dbar = b * 2 + dh if PLANTED != "d_full_by_buffer" else b * 2
                 yield from wait(d_full[dbar], seen[b], f"D{dh}{q} k{k}")
                 seen[b] += 1
-                s_ = k % N_SQ
-                yield from wait(sq_full[s_ * 2 + dh], sq_seen[s_], f"D{dh}{q} k{k} sq")
-                sq_seen[s_] += 1
+                s_ = k % (3 if PLANTED == "sq_col_mod3" else N_SQ)
                 check(k in mma_done, f"D of chunk {k} read before its MMAs completed")
+                check(sq_col.get((s_, q)) == k, f"chunk {k} read its sum column holding chunk {sq_col.get((s_, q))}")
                 yield None
                 d_read[k] += 1
                 sq_read[k] += 1
-                chunk_done[s_ * 2 + dh].arrive()
                 mma_ready[b].arrive()  # D buffer b free for chunk k + 3
             j = sl[i] - s_first
             if j + SLOTS < n_sl and (i == n - 1 or sl[i + 1] != sl[i]):
@@ -242,12 +237,14 @@ def test_protocol_sound_and_deadlock_free(M, K):
                 assert not errs, f"M={M} K={K} units {ub}+{n} seed {seed}: {errs[:3]}"
 
 
-@pytest.mark.parametrize("mistake", ["wrong_a_buffer", "d_full_by_buffer", "refill_no_wait"])
+@pytest.mark.parametrize("mistake", ["wrong_a_buffer", "d_full_by_buffer", "refill_no_wait",
+                                     "sq_col_mod3"])
 def test_model_catches_planted_mistakes(mistake):
     """The checks have teeth: a transform third that waits on another third's
     A barrier, accumulate halves that share one D barrier per buffer (each
-    then sees only some of its phases), or a refilled W slot marked full by
-    the half's first warp without waiting for the other three, are reported
+    then sees only some of its phases), a refilled W slot marked full by
+    the half's first warp without waiting for the other three, or sum-of-
+    squares columns reused every three chunks instead of six, are reported
     (an early return, a buffer rewritten or used too soon, or the deadlock
     they lead to)."""
     global PLANTED
