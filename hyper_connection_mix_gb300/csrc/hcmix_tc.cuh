@@ -43,8 +43,10 @@
 // written, MMAs issued and completed, rewritten; D buffer: MMAs completed,
 // read, next MMAs issued) spans fewer than three chunks.  Every mbarrier wait
 // is by a waiter that has seen the barrier's previous phase, as a parity wait
-// needs: each A buffer, D buffer (per accumulate half) and x stage slot has
-// fixed waiters that see every phase.  The sums of squares need no barrier of
+// needs: each D barrier (per buffer and accumulate half) and x stage slot
+// has fixed waiters that see every phase (the MMA commit that completes a D
+// barrier also frees the chunk's A buffer, for the transform third that
+// wrote it).  The sums of squares need no barrier of
 // their own: column 480 + k % 6 is written with chunk k's A (before its MMAs
 // are issued) and read with its D (after they complete), and it is written
 // again for chunk k + 6 only after the MMAs of chunk k + 3 completed, which
@@ -148,7 +150,6 @@ constexpr size_t kSmemBytes = kBkOff<kTf32> + 1024 + 1024;  // bookkeeping + bas
 struct Bookkeeping {
   uint64_t full_x[kXStages];
   uint64_t empty_x[kXStages];
-  uint64_t a_empty[kNumA];  // [k % 3]: the MMAs of chunk k are done (A buffer free)
   uint64_t mma_ready[kNumMma];  // chunk k (issuer k % 3): A(k) written and D(k - 3) read
   uint64_t d_full[kNumD * 2];  // [b * 2 + (k / 4) % 2]: D buffer b holds chunk k, of accumulate half (k / 4) % 2
   uint64_t w_full[kWBufs];
@@ -167,7 +168,7 @@ static_assert(kDCol0 + kNumD * kDCols<false> <= kSqCol0 &&
                   kDCol0 + kNumD * kDCols<true> <= kSqCol0 && kSqCol0 + kNumSq <= kTmemCols,
               "TMEM budget");
 static_assert(sizeof(Bookkeeping) <= 1024, "bookkeeping area");
-static_assert(3 + 3 + 6 + 6 <= 30,
+static_assert(3 + 6 + 6 <= 30,
               "one barrier (pair) per lane of the initialising warp; lanes 30 and 31 do the rest");
 static_assert(kChunksPerSlice % kChunksPerStage == 0, "x stages hold chunks of one unit");
 static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "dynamic shared memory");
@@ -884,12 +885,10 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       mbar_init(smem_u32(&bk.mma_ready[lane]), 8);
       for (int q = 0; q < 4; ++q) mbar_arrive(smem_u32(&bk.mma_ready[lane]));
       mbar_init(smem_u32(&bk.drain[lane]), 1);
-    } else if (lane < kNumMma + kNumA) {
-      mbar_init(smem_u32(&bk.a_empty[lane - kNumMma]), 1);  // MMA commit
-    } else if (lane < kNumMma + kNumA + 2 * kNumD) {
-      mbar_init(smem_u32(&bk.d_full[lane - kNumMma - kNumA]), 1);  // MMA commit
-    } else if (lane < kNumMma + kNumA + 2 * kNumD + kTailSlots) {
-      mbar_init(smem_u32(&bk.tail_bar[lane - kNumMma - kNumA - 2 * kNumD]), 1);
+    } else if (lane < kNumMma + 2 * kNumD) {
+      mbar_init(smem_u32(&bk.d_full[lane - kNumMma]), 1);  // MMA commit
+    } else if (lane < kNumMma + 2 * kNumD + kTailSlots) {
+      mbar_init(smem_u32(&bk.tail_bar[lane - kNumMma - 2 * kNumD]), 1);
     } else if (lane == 30) {
       for (int h = 0; h < 2; ++h) mbar_init(smem_u32(&bk.refill_done[h]), 4);  // the half's four warps
     } else if (lane == 31) {
@@ -931,9 +930,9 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // so the wait returns at once after the first).  mma_ready[t] is this
     // warp's own barrier, so it has seen every earlier phase, as a parity
     // wait needs; a W barrier's earlier fill has always completed before any
-    // issuer waits for its next one.  Each chunk commits twice: D complete
-    // (d_full) and A free again (a_empty).  The whole warp runs the loop, the
-    // waits are warp votes and one elected lane issues each MMA and commit.
+    // issuer waits for its next one.  Each chunk commits once, on d_full:
+    // D complete and A free again.  The whole warp runs the loop, the waits
+    // are warp votes and one elected lane issues each MMA and the commit.
     const int t = warp - kMmaWarp0;
     bool ok = true;
     UnitCursor u = cursor0;
@@ -955,7 +954,6 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         mma_chunk_tf32x3(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t * 2 + (i & 1)]));
       else
         mma_chunk_exact(d, a, bdesc, MD::kIdesc, smem_u32(&bk.d_full[t * 2 + (i & 1)]));
-      umma_commit_warp(smem_u32(&bk.a_empty[t]));
     }
     if (!ok && lane == 0) fail(bk, P.err);
     // every MMA this warp issued completes before TMEM is released
@@ -993,13 +991,17 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     // returns at once.  Every wait below follows that rule: with three x stages
     // of two chunks, stage slot L % 3 always holds chunks of the same two
     // thirds, so this third waits for every phase of the slots it uses; and
-    // a_empty[tt] carries only this third's chunks.
+    // the MMAs of its own previous chunk k - 3 complete on d_full[tt][h], h =
+    // ((k - 3) / 4) % 2: every phase of d_full[tt][0] and [1] is a chunk of
+    // this third, waited for in order, and none can complete past chunk k - 3
+    // before this third has written chunk k's A.
     const int tt = (warp - kFirstTWarp) >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t a_col = tmem + (uint32_t)tt * kACols;
     const uint32_t row_sw = (uint32_t)row * kRowBytes + ((uint32_t)(row & 7) << 4);
+    uint32_t ae_par = 0;  // bit h: parity of the next phase of d_full[tt][h] this third waits for
     bool ok = true;
     for (int k = tt; k < n_chunks; k += kNumA) {
       const int L = k / kChunksPerStage, st = L % kXStages;
@@ -1050,9 +1052,10 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       // column s: the accumulate warps read chunk k - 6's column before they
       // freed D for chunk k - 3's MMAs
       if (k >= kNumA) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.a_empty[tt]),
-                                               (uint32_t)(k / kNumA - 1) & 1u, abort_flag,
-                                               kWaitLimitNs));
+        const int h = ((k - kNumA) / kChunksPerSlice) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bk.d_full[tt * 2 + h]),
+                                               (ae_par >> h) & 1u, abort_flag, kWaitLimitNs));
+        ae_par ^= 1u << h;
         if (!ok) break;
       }
       tc_fence_after();

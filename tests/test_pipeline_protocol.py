@@ -59,7 +59,6 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     for b in mma_ready:
         for _ in range(4):
             b.arrive()
-    a_empty = mk("a_empty", 1, N_A)  # [k % 3]: chunk k's MMAs done
     # d_full[b * 2 + h]: D buffer b holds a chunk of accumulate half h
     d_full, w_full = mk("d_full", 1, 2 * N_D), mk("w_full", 1, 4 * SLOTS)
     dconv = Bar(8, "dconv")
@@ -98,6 +97,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
             yield None
 
     def transform(tt, q):  # the chunks k with k % 3 == tt
+        ae_seen = [0, 0]  # phases of d_full[tt * 2 + h] waited for so far
         for k in range(tt, nck, N_A):
             L, st = k // 2, (k // 2) % X_STAGES
             s_ = k % (3 if PLANTED == "sq_col_mod3" else N_SQ)
@@ -105,9 +105,11 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
             yield None
             x_read[L] += 1
             empty_x[st].arrive()
-            if k >= N_A:  # chunk k - 3 (this third's) is done with A buffer tt
+            if k >= N_A:  # chunk k - 3 (this third's) is done with A buffer tt: its D commit
+                h = ((k - N_A) // 4) % 2
                 a = (tt + 1) % N_A if PLANTED == "wrong_a_buffer" else tt
-                yield from wait(a_empty[a], k // N_A - 1, f"T{tt}{q} k{k} A")
+                yield from wait(d_full[a * 2 + h], ae_seen[h], f"T{tt}{q} k{k} A")
+                ae_seen[h] += 1
                 check(k - N_A in mma_done, f"A buffer of chunk {k} rewritten before the MMAs of {k - N_A} were done")
             # the A limbs and the sum of squares into TMEM
             old = sq_col.get((s_, q))
@@ -195,7 +197,6 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
                 k, dbar = pipe.pop(0)  # the tensor pipe completes MMAs in issue order
                 mma_done.add(k)
                 d_full[dbar].arrive()
-                a_empty[k % N_A].arrive()
             else:
                 st, _ = tma.pop(rnd.randrange(len(tma)))
                 full_x[st].arrive()
