@@ -19,8 +19,8 @@
 //     (the first 24 columns exact; x1.w3 ~ 2^-34 relative is dropped);
 //   * warp 3 (one lane), the x producer: it initialises the x barriers,
 //     TMA-loads the fp32 W of the CTA's first two slices (staged in slot 1's
-//     buffers) and then x, two chunks of a tile (32 KB, 128-byte swizzle) per
-//     load into a 3-stage ring.  It issues nothing else, so no other role's
+//     buffers) and then x, one chunk of a tile (16 KB, 128-byte swizzle) per
+//     load into a 6-stage ring.  It issues nothing else, so no other role's
 //     shared-memory accesses queue behind its copies;
 //   * warps 4..15, the transform warps, three thirds of four (one per
 //     quadrant): third t takes the chunks with k % 3 == t.  Each thread reads
@@ -82,8 +82,11 @@
 namespace hcmix {
 namespace tc {
 
-constexpr int kXStages = 3;        // x stages in flight
-constexpr int kChunksPerStage = 2;  // an x stage holds two chunks of a tile (one 32 KB load)
+// x stages in flight, each one chunk of a tile (one 16 KB load): stage k % 6
+// holds chunk k, so each stage serves one transform third.  (Three stages of
+// two chunks stream as fast; the smaller first loads land sooner.)
+constexpr int kXStages = 6;
+constexpr int kChunksPerStage = 1;
 constexpr int kNumA = 3;   // TMEM A buffers: chunk k uses A buffer k % 3 (transform third k % 3)
 constexpr int kNumD = 3;   // TMEM D buffers: chunk k uses D buffer k % 3
 constexpr int kNumSq = 6;  // sum-of-squares TMEM columns: chunk k uses kSqCol0 + k % 6
@@ -180,7 +183,7 @@ static_assert(kNumTWarps == 3 * 4 && kFirstTWarp % 4 == 0 && kFirstDWarp % 4 == 
                   (kFirstTWarp + kNumTWarps <= kFirstDWarp || kFirstDWarp + kNumDWarps <= kFirstTWarp),
               "warp roles");
 static_assert(kNumMma == 3 && kNumA == 3 && kNumD == 3 && kNumTWarps == 12 && kNumDWarps == 8 &&
-                  kNumSq % 3 == 0 && kXStages == 3 && kChunksPerStage == 2 &&
+                  kNumSq % 3 == 0 && kXStages * kChunksPerStage == 6 &&
                   kXWarp < kFirstWorkWarp && kMmaWarp0 + kNumMma <= kFirstWorkWarp &&
                   (kXWarp < kMmaWarp0 || kXWarp >= kMmaWarp0 + kNumMma),
               "issuer k % 3 and transform third k % 3 own A buffer k % 3 (so a stage slot "
@@ -748,14 +751,15 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   // at a time (no division per chunk)
   const UnitCursor cursor0{0, tile0, s_first};
 
-  // x load L fills stage L % kXStages with chunks 2L and 2L + 1 (unit L / 2,
-  // at which `u` stands)
+  // x load L fills stage L % kXStages with chunks kChunksPerStage L .. (unit
+  // L / kLoadsPerUnit, at which `u` stands)
+  constexpr int kLoadsPerUnit = kChunksPerSlice / kChunksPerStage;
   auto issue_x_load = [&](int L, const UnitCursor& u, uint64_t pol) {
     const int st = L % kXStages;
     const uint32_t full = smem_u32(&bk.full_x[st]);
     mbar_arrive_expect_tx(full, kXBytes);
     tma_load_3d(x_base + (uint32_t)st * kXBytes, &tmap_x, 0, u.tile * kTileM,
-                u.slice * kChunksPerSlice + (L % 2) * kChunksPerStage, full, pol);
+                u.slice * kChunksPerSlice + (L % kLoadsPerUnit) * kChunksPerStage, full, pol);
   };
   // limbs of chunk c of slice s into W buffer (slot, c) by TMA (exact mode)
   auto issue_w_load = [&](int slot, int c, int s, uint64_t pol) {
@@ -969,7 +973,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
       int L = 1;
       for (; L < n_loads; ++L) {
         const int st = L % kXStages;
-        u.advance_to(L / 2, P.n_tiles);
+        u.advance_to(L / kLoadsPerUnit, P.n_tiles);
         if (L >= kXStages && !mbar_wait(smem_u32(&bk.empty_x[st]), (uint32_t)(L / kXStages - 1) & 1u, abort_flag,
                        kWaitLimitNs)) {
           fail(bk, P.err);
@@ -984,13 +988,13 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
   } else if (warp >= kFirstTWarp && warp < kFirstTWarp + kNumTWarps) {
     // ---------------- transform warps, three thirds of four (one warp per
-    // quadrant each): third tt takes the chunks k with k % 3 == tt, from half
-    // k % 2 of x load k / 2, into A buffer tt.  A parity wait for phase p of an
+    // quadrant each): third tt takes the chunks k with k % 3 == tt, from x
+    // load k (stage k % 6), into A buffer tt.  A parity wait for phase p of an
     // mbarrier is only sound when the waiter already knows phase p - 1
     // complete: earlier, the wait cannot tell p - 2 (same parity) from p and
-    // returns at once.  Every wait below follows that rule: with three x stages
-    // of two chunks, stage slot L % 3 always holds chunks of the same two
-    // thirds, so this third waits for every phase of the slots it uses; and
+    // returns at once.  Every wait below follows that rule: stage k % 6 always
+    // holds chunks of the same third, so this third waits for every phase of
+    // the stages it uses; and
     // the MMAs of its own previous chunk k - 3 complete on d_full[tt][h], h =
     // ((k - 3) / 4) % 2: every phase of d_full[tt][0] and [1] is a chunk of
     // this third, waited for in order, and none can complete past chunk k - 3

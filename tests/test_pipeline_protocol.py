@@ -26,7 +26,7 @@ import random
 
 import pytest
 
-X_STAGES, N_A, N_D, N_SQ, SLOTS, N_MMA = 3, 3, 3, 6, 2, 3
+X_STAGES, CPS, N_A, N_D, N_SQ, SLOTS, N_MMA = 6, 1, 3, 3, 6, 2, 3  # CPS: chunks per x stage
 PLANTED = None  # a planted mistake for the tests that check the model has teeth
 
 
@@ -50,9 +50,9 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     sl = [(u_begin + i) // n_tiles for i in range(n)]
     s_first = sl[0]
     n_sl = sl[-1] - s_first + 1
-    nck, nld = 4 * n, 2 * n
+    nck, nld = 4 * n, 4 * n // CPS
     mk = lambda p, c, m: [Bar(c, f"{p}{i}") for i in range(m)]
-    full_x, empty_x = mk("full_x", 1, X_STAGES), mk("empty_x", 8, X_STAGES)
+    full_x, empty_x = mk("full_x", 1, X_STAGES), mk("empty_x", 4 * CPS, X_STAGES)
     # mma_ready[k % 3]: the four transform warps of chunk k and the four
     # accumulate warps that have read chunk k - 3 (made at set-up for k < 3)
     mma_ready = mk("mma_ready", 8, N_MMA)
@@ -86,7 +86,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
             errors.append(what)
 
     def issue_load(L):
-        check(L < X_STAGES or x_read[L - X_STAGES] == 8, f"x load {L} over an unread stage")
+        check(L < X_STAGES or x_read[L - X_STAGES] == 4 * CPS, f"x load {L} over an unread stage")
         tma.append((L % X_STAGES, L))
 
     def x_producer():  # the loads after the first (set-up issues load 0)
@@ -99,7 +99,7 @@ def run_cta(u_begin, n, n_tiles, seed, packed=False):
     def transform(tt, q):  # the chunks k with k % 3 == tt
         ae_seen = [0, 0]  # phases of d_full[tt * 2 + h] waited for so far
         for k in range(tt, nck, N_A):
-            L, st = k // 2, (k // 2) % X_STAGES
+            L, st = k // CPS, (k // CPS) % X_STAGES
             s_ = k % (3 if PLANTED == "sq_col_mod3" else N_SQ)
             yield from wait(full_x[st], L // X_STAGES, f"T{tt}{q} k{k} x")
             yield None
