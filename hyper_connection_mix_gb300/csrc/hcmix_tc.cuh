@@ -515,24 +515,32 @@ __device__ __forceinline__ void fail(Bookkeeping& bk, uint32_t* err) {
   *reinterpret_cast<volatile int*>(&bk.abort) = 1;
 }
 
-// Grid-wide barrier on a monotonic 64-bit counter in the workspace header,
-// called by one thread per CTA after a CTA barrier that follows the CTA's
-// stores.  Every launch adds exactly kBarrierQuantum to it (each CTA 1, CTA 0
-// also the kBarrierQuantum - G of the CTAs the grid does not have), so at the
-// start of a launch it is a multiple of kBarrierQuantum, and any value a CTA
-// reads before its own arrival lies below the next multiple: `base` is that
-// value rounded down, and the barrier opens when the counter reaches base +
-// kBarrierQuantum.  The arrival is a release add at GPU scope (it publishes the
-// CTA's stores), the wait a bounded loop of acquire loads.  Every CTA must be
-// resident (cooperative launch).  Returns false when the wait ran out.
-constexpr unsigned long long kBarrierQuantum = 1024;  // above any grid size
+// Grid-wide barrier on a monotonic 64-bit counter in the workspace header.
+// Every launch that has a tail adds exactly kBarrierQuantum to it, so at the
+// start of a launch it is a multiple of kBarrierQuantum, and any value a
+// thread reads before its own arrival lies below the next multiple: `base`
+// is that value rounded down, and the barrier opens when the counter reaches
+// base + kBarrierQuantum.  Arrivals are release adds at GPU scope (each
+// publishes the stores its thread has made or synchronised with).  Above
+// eight rows each of a CTA's eight accumulate warps arrives (lane 0, after a
+// warp sync) as soon as it has stored its last partials, 1 each, and the
+// first of CTA 0 also adds the kBarrierQuantum - 8 G of the warps the grid
+// does not have; one thread per CTA then waits (grid_barrier_wait: a bounded
+// loop of acquire loads).  Up to eight rows one thread per CTA adds the CTA's
+// share (grid_barrier_add) after a CTA barrier.  Every CTA must be resident
+// (cooperative launch).
+constexpr unsigned long long kBarrierQuantum = 8192;  // above 8 x any grid size
 
 __device__ __forceinline__ unsigned long long grid_barrier_add(int64_t b, int64_t nblocks) {
   return b == 0 ? 1 + kBarrierQuantum - (unsigned long long)nblocks : 1;
 }
-__device__ __forceinline__ bool grid_barrier(unsigned long long* counter, unsigned long long base,
-                                             int64_t b, int64_t nblocks, uint64_t limit_ns) {
-  sm100::red_add_release_gpu_u64(counter, grid_barrier_add(b, nblocks));
+__device__ __forceinline__ unsigned long long grid_barrier_warp_add(int64_t b, int dtid,
+                                                                    int64_t nblocks) {
+  return b == 0 && dtid == 0 ? 1 + kBarrierQuantum - 8 * (unsigned long long)nblocks : 1;
+}
+// Returns false when the wait ran out.
+__device__ __forceinline__ bool grid_barrier_wait(const unsigned long long* counter,
+                                                  unsigned long long base, uint64_t limit_ns) {
   const unsigned long long target = base + kBarrierQuantum;
   const uint64_t t0 = sm100::global_timer_ns();
   for (uint32_t i = 0; sm100::ld_acquire_gpu_u64(counter) < target; ++i) {
@@ -1223,6 +1231,11 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         refill(j + kSlots);
     }
     if (!ok) fail(bk, P.err);
+    if (P.tail != 0 && P.M > 8) {  // this warp's arrival at the grid barrier
+      static_assert(kNumDWarps == 8, "eight arrivals per CTA");
+      __syncwarp();
+      if (lane == 0) red_add_release_gpu_u64(P.gbar, grid_barrier_warp_add(b, dtid, G));
+    }
     if constexpr (!kTf32) {
       // the TMA loads of prepacked limbs complete before the CTA can exit
       if (P.w_src == nullptr && dtid == 0)
@@ -1270,7 +1283,7 @@ hcmix_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
   tail_params(P, smem);
   const TailPlan T(P, b, G);
   if (threadIdx.x == 0) {
-    if (!grid_barrier(P.gbar, bk.gbar_base, b, G, kWaitLimitNs))
+    if (!grid_barrier_wait(P.gbar, bk.gbar_base, kWaitLimitNs))
       record_device_error(P.err, kDevWaitTimeout);
     tail_start(P, T, smem, bk.tail_bar);
   }
