@@ -60,6 +60,56 @@ __device__ __forceinline__ float rsqrt_fast(float v) {
 // reciprocal, which leaves an infinity or NaN in the matrix: the caller checks
 // for that and redoes the rounds with kDivide, which divides each entry by
 // its sum (IEEE, as the oracle does) instead.
+// The same rounds (hc_eps = 0) in scaling form: the matrix A = exp of the
+// logits stays as it is and the rounds update a row scale u and a column
+// scale v instead, u_i = 1 / sum_j A_ij v_j, then v_j = 1 / sum_i A_ij u_i;
+// after the last round the result is A_ij u_i v_j.  In exact arithmetic this
+// is the row-then-column normalisation above: after every step the
+// normalised matrix is A_ij u_i v_j, and normalising its rows (columns) sets
+// u (v) as written.  It leaves one reciprocal per sum and no per-entry
+// scaling in the chain, so a round is ~10% shorter.  Each sum is formed in
+// pairs, (A_i0 v_0 + A_i2 v_2) + (A_i1 v_1 + A_i3 v_3).  A scale that is not
+// a positive finite number (a sum that overflowed, or reached 2^126, where the
+// approximate reciprocal flushes to zero, or fell below the normal range)
+// turns the result into NaN, so that the caller's check redoes the rounds
+// with kDivide.
+__device__ __forceinline__ void sinkhorn_rounds_scaled(float2 (&P)[kHc][kHc / 2], int iters) {
+  static_assert(kHc == 4, "four-by-four comb");
+  float u[kHc] = {1.0f, 1.0f, 1.0f, 1.0f};
+  float2 v[kHc / 2] = {make_float2(1.0f, 1.0f), make_float2(1.0f, 1.0f)};
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < kHc; ++i) {
+      const float2 t = __ffma2_rn(P[i][1], v[1], __fmul2_rn(P[i][0], v[0]));
+      u[i] = rcp_fast(__fadd_rn(t.x, t.y));
+    }
+#pragma unroll
+    for (int h = 0; h < kHc / 2; ++h) {
+      const float2 a = __ffma2_rn(P[1][h], make_float2(u[1], u[1]),
+                                  __fmul2_rn(P[0][h], make_float2(u[0], u[0])));
+      const float2 b = __ffma2_rn(P[3][h], make_float2(u[3], u[3]),
+                                  __fmul2_rn(P[2][h], make_float2(u[2], u[2])));
+      const float2 c = __fadd2_rn(a, b);
+      v[h] = make_float2(rcp_fast(c.x), rcp_fast(c.y));
+    }
+  }
+  if (iters > 0) {
+    bool good = true;
+#pragma unroll
+    for (int i = 0; i < kHc; ++i) good = good && u[i] > 0.0f && u[i] <= 3.40282347e38f;
+#pragma unroll
+    for (int h = 0; h < kHc / 2; ++h)
+      good = good && v[h].x > 0.0f && v[h].x <= 3.40282347e38f && v[h].y > 0.0f &&
+             v[h].y <= 3.40282347e38f;
+    if (!good) u[0] = __int_as_float(0x7fc00000);  // NaN: the caller redoes the rounds
+#pragma unroll
+    for (int i = 0; i < kHc; ++i)
+#pragma unroll
+      for (int h = 0; h < kHc / 2; ++h)
+        P[i][h] = __fmul2_rn(__fmul2_rn(P[i][h], make_float2(u[i], u[i])), v[h]);
+  }
+}
+
 template <bool kDivide, bool kEps>
 __device__ __forceinline__ void sinkhorn_rounds(float2 (&P)[kHc][kHc / 2], int iters, float hc_eps) {
   static_assert(kHc == 4, "four-by-four comb");
@@ -142,7 +192,7 @@ __device__ __forceinline__ void epilogue_row4(const float (&s_tot)[kPartStride][
   if (hc_eps != 0.0f)
     sinkhorn_rounds<false, true>(P, iters, hc_eps);
   else
-    sinkhorn_rounds<false, false>(P, iters, hc_eps);
+    sinkhorn_rounds_scaled(P, iters);
   float check = 0.0f;
 #pragma unroll
   for (int i = 0; i < kHc; ++i) check += (P[i][0].x + P[i][0].y) + (P[i][1].x + P[i][1].y);

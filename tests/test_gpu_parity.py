@@ -246,6 +246,24 @@ def test_sinkhorn_row_below_the_normal_range(path):
     check_all(x, hi.make_w(K=K), hi.make_scale(), bs, path, "subnormal comb row")
 
 
+def test_sinkhorn_sums_near_the_top_of_the_range(path):
+    """Comb rows whose exponentials are near the top of the fp32 range (logits of
+    86.2 to 87, x = 0 so logit = hc_base): their sums lie between 2^126, where an
+    approximate reciprocal flushes to zero, and the largest finite float, so the
+    oracle's results are finite; the epilogue notices the zero scale and
+    divides by the sums instead, and the results match the oracle."""
+    K = 1024
+    x = np.zeros((12, K), np.uint16)
+    bs = hi.make_base()
+    bs[8:12] = np.float32(87.0)
+    bs[12:16] = np.float32(86.5)
+    bs[16:20] = np.float32(86.2)
+    bs[20:24] = np.float32(86.8)
+    got = run(x, hi.make_w(K=K), hi.make_scale(), bs, path)
+    assert all(np.isfinite(g).all() for g in got[:3])
+    check_all(x, hi.make_w(K=K), hi.make_scale(), bs, path, "comb sums near the top")
+
+
 def test_nonfinite_inputs_propagate(path):
     """A NaN or an infinity in a row of x carries into that row's outputs (each
     output non-finite where the oracle's is), the other rows are unaffected,
